@@ -1,0 +1,252 @@
+/*
+ * loco_oracle.c — TEST INFRASTRUCTURE ONLY.  A plain, slow, element-by-element
+ * CPU statement of what the LoCo hot path computes, used to check the CUDA
+ * library.  Only the test suite, the smoke check and the benchmark's CPU
+ * baseline load it; no product code path may call it.  It shares no source,
+ * header or constant with the CUDA library.
+ *
+ * Method: "LoCo: Low-Bit Communication Adaptor for Large-scale Model
+ * Training" (arXiv 2407.04480), §3.1 Eqns (1)-(3), §3.2 Eqns (4)-(7),
+ * §3.3 Eqn (8), §4 Eqn (9).  The displayed equations were lost from the
+ * available text; each function states the reading it implements.
+ *
+ * Precision: IEEE binary32 throughout, round to nearest even, every product
+ * and sum a separate rounded operation.  Build with -ffp-contract=off and
+ * without -ffast-math (gcc contracts a*b+c into fma by default on aarch64).
+ * fp64 appears only in the shadow sum of oracle_decode_reduce and in the
+ * bias-correction constants of the Adam step, as stated there.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits. */
+static float bf16_bits_to_f32(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Round_p-bit of Eqn (1): nearest integer, halves to even (the rounding of
+ * torch.round, "the default one in PyTorch", §3.1), saturated to
+ * [-2^(p-1), 2^(p-1)-1].  Saturating first and rounding second gives the same
+ * integer because both bounds are integers and rounding is monotone. */
+static int round_pbit(float x, int bits) {
+  float qmax = (float)((1 << (bits - 1)) - 1);
+  float qmin = -(float)(1 << (bits - 1));
+  if (x < qmin) x = qmin;
+  if (x > qmax) x = qmax;
+  return (int)nearbyintf(x); /* default rounding mode: nearest, ties to even */
+}
+
+/* Read one gradient element as fp32. */
+static float grad_at(const void* grad, int grad_is_bf16, int64_t i) {
+  if (grad_is_bf16) return bf16_bits_to_f32(((const uint16_t*)grad)[i]);
+  return ((const float*)grad)[i];
+}
+
+/* Store the p-bit two's-complement code q of element j (index within its
+ * block) into the block's packed bytes. */
+static void put_code(uint8_t* blk, int bits, int j, int q) {
+  if (bits == 8) {
+    blk[j] = (uint8_t)(q & 0xFF);
+  } else {
+    uint8_t nib = (uint8_t)(q & 0xF);
+    if (j % 2 == 0)
+      blk[j / 2] = (uint8_t)((blk[j / 2] & 0xF0) | nib);
+    else
+      blk[j / 2] = (uint8_t)((blk[j / 2] & 0x0F) | (nib << 4));
+  }
+}
+
+/* Read back the code of element j of a block (sign-extended). */
+static int get_code(const uint8_t* blk, int bits, int j) {
+  if (bits == 8) return (int)(int8_t)blk[j];
+  int nib = (j % 2 == 0) ? (blk[j / 2] & 0xF) : (blk[j / 2] >> 4);
+  return nib >= 8 ? nib - 16 : nib;
+}
+
+/*
+ * Sender step of LoCo for the quant blocks [b0, b1) of a bucket of n elements.
+ *
+ *  §3.1 Eqn (2):  h = g + decompressor(e)           (e stored in fp32 here)
+ *  §3.1 Eqns (1),(3): c = Round_p-bit(s*h); this build chooses s per block as
+ *                 qmax/A_b (A_b = max|h| of the block), or one fixed s for all
+ *                 blocks; the decompressor multiplies the code by Delta = 1/s.
+ *  §3.2 Eqn (4),(5): error moving average  e~ = beta*e~_prev + (1-beta)*(h-d)
+ *  §3.2 Eqn (7):  the error is held within the range of the 8-bit compressor
+ *                 of scale s_e = kappa*s, i.e. [-128/s_e, 127/s_e], and set to
+ *                 zero every T_c steps.
+ *
+ * fixed_mode: 0 = per-block absmax, 1 = fixed scale s = fixed_scale.
+ * err is updated in place for the elements of the processed blocks.
+ * codes holds all blocks' packed codes (block b at byte b*block*bits/8);
+ * scales[b] receives Delta_b.
+ */
+void oracle_compress(int bits, int block, int fixed_mode, float fixed_scale,
+                     float beta, float kappa, int64_t reset_period,
+                     const void* grad, int grad_is_bf16, float* err, int64_t n,
+                     int64_t step, uint8_t* codes, float* scales,
+                     int64_t b0, int64_t b1) {
+  const float qmax = (float)((1 << (bits - 1)) - 1);
+  const float one_minus_beta = 1.0f - beta;
+  const int reset = (reset_period > 0) && (step % reset_period == 0);
+  const int64_t bytes_per_block = (int64_t)block * bits / 8;
+  float h[1024]; /* block <= 1024 */
+
+  for (int64_t b = b0; b < b1; ++b) {
+    const int64_t lo = b * block;
+    int64_t cnt = n - lo;
+    if (cnt > block) cnt = block;
+
+    /* Eqn (2): compensate. */
+    for (int64_t j = 0; j < cnt; ++j) {
+      float g = grad_at(grad, grad_is_bf16, lo + j);
+      h[j] = g + err[lo + j];
+    }
+
+    /* Scale of Eqn (1) for this block. */
+    float delta, inv;
+    if (fixed_mode) {
+      delta = 1.0f / fixed_scale;
+      inv = fixed_scale;
+    } else {
+      float amax = 0.0f;
+      for (int64_t j = 0; j < cnt; ++j) {
+        float a = fabsf(h[j]);
+        if (a > amax) amax = a;
+      }
+      if (amax == 0.0f) {
+        delta = 0.0f;
+        inv = 0.0f;
+      } else {
+        delta = amax / qmax;
+        inv = qmax / amax;
+      }
+    }
+    scales[b] = delta;
+
+    /* Bounds of the 8-bit error compressor, scale s_e = kappa*s (Eqn 7). */
+    const float delta_e = delta / kappa;
+    const float e_lo = -128.0f * delta_e;
+    const float e_hi = 127.0f * delta_e;
+
+    uint8_t* blk = codes + b * bytes_per_block;
+    for (int j = 0; j < block; ++j) {
+      if (j >= cnt) { /* ragged tail: padding elements get code 0 */
+        put_code(blk, bits, j, 0);
+        continue;
+      }
+      /* Eqns (1),(3): low-bit code. */
+      float x = h[j] * inv;
+      int q = round_pbit(x, bits);
+      put_code(blk, bits, j, q);
+      /* Eqn (4): decompressed value and this step's compression error. */
+      float d = (float)q * delta;
+      float r = h[j] - d;
+      /* Eqn (5): moving average with the stored previous error. */
+      float prev = err[lo + j];
+      float t1 = beta * prev;
+      float t2 = one_minus_beta * r;
+      float t = t1 + t2;
+      /* Eqn (7): saturation of the 8-bit error compressor, then reset. */
+      if (t < e_lo) t = e_lo;
+      if (t > e_hi) t = e_hi;
+      if (reset) t = 0.0f;
+      err[lo + j] = t;
+    }
+  }
+}
+
+/*
+ * Receiver step, §3.3 Eqn (8): decompress every rank's codes and average them
+ * in high precision, for elements [i0, i1) of a bucket.  Each term is
+ * f32(q)*Delta; the terms are summed in rank order 0..W-1 in fp32 and the sum
+ * is divided by W.  If mean64 is not NULL it receives the same average formed
+ * in fp64 from the same fp32 terms (for measuring rounding error).
+ */
+void oracle_decode_reduce(int bits, int block, const uint8_t* const* codes,
+                          const float* const* scales, int W, int64_t i0, int64_t i1,
+                          float* mean, double* mean64) {
+  const int64_t bytes_per_block = (int64_t)block * bits / 8;
+  for (int64_t i = i0; i < i1; ++i) {
+    const int64_t b = i / block;
+    const int j = (int)(i % block);
+    float acc = 0.0f;
+    double acc64 = 0.0;
+    for (int w = 0; w < W; ++w) {
+      int q = get_code(codes[w] + b * bytes_per_block, bits, j);
+      float d = (float)q * scales[w][b];
+      acc = (w == 0) ? d : acc + d;
+      acc64 += (double)d;
+    }
+    mean[i] = acc / (float)W;
+    if (mean64) mean64[i] = acc64 / (double)W;
+  }
+}
+
+/*
+ * Receiver step fused with the optimizer, §4 Eqn (9): the averaged low-bit
+ * gradient g~ of Eqn (8) drives one Adam(W) update of param, m, v for the
+ * elements [i0, i1).  g~ is formed exactly as in oracle_decode_reduce.
+ * The update (Kingma & Ba's Adam with decoupled weight decay):
+ *   p = p - (lr*wd)*p ; m = beta1*m + (1-beta1)*g ; v = beta2*v + (1-beta2)*g*g
+ *   mh = m/bc1 ; vh = v/bc2 ; den = sqrt(vh)+eps (or sqrt(vh+eps)) ;
+ *   p = p - lr*(mh/den)
+ * bc1, bc2 are 1 - beta^t computed in double and rounded to fp32, or 1 when
+ * bias correction is off.
+ */
+void oracle_adam_step(int bits, int block, const uint8_t* const* codes,
+                      const float* const* scales, int W, int64_t i0, int64_t i1,
+                      float* param, float* m, float* v,
+                      float lr, float beta1, float beta2, float eps, float wd,
+                      int bias_correction, int eps_inside_sqrt, int64_t t) {
+  const int64_t bytes_per_block = (int64_t)block * bits / 8;
+  const float lr_wd = lr * wd;
+  const float omb1 = 1.0f - beta1;
+  const float omb2 = 1.0f - beta2;
+  float bc1 = 1.0f, bc2 = 1.0f;
+  if (bias_correction) {
+    bc1 = (float)(1.0 - pow((double)beta1, (double)t));
+    bc2 = (float)(1.0 - pow((double)beta2, (double)t));
+  }
+  for (int64_t i = i0; i < i1; ++i) {
+    const int64_t b = i / block;
+    const int j = (int)(i % block);
+    float acc = 0.0f;
+    for (int w = 0; w < W; ++w) {
+      int q = get_code(codes[w] + b * bytes_per_block, bits, j);
+      float d = (float)q * scales[w][b];
+      acc = (w == 0) ? d : acc + d;
+    }
+    float g = acc / (float)W;
+
+    float p = param[i];
+    float decay = lr_wd * p;
+    p = p - decay;
+    float mi = beta1 * m[i];
+    float mg = omb1 * g;
+    mi = mi + mg;
+    float gg = g * g;
+    float vi = beta2 * v[i];
+    float vg = omb2 * gg;
+    vi = vi + vg;
+    float mh = mi / bc1;
+    float vh = vi / bc2;
+    float den;
+    if (eps_inside_sqrt) {
+      float s = vh + eps;
+      den = sqrtf(s);
+    } else {
+      float s = sqrtf(vh);
+      den = s + eps;
+    }
+    float ratio = mh / den;
+    float step = lr * ratio;
+    p = p - step;
+    param[i] = p;
+    m[i] = mi;
+    v[i] = vi;
+  }
+}
