@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the LoCo data-parallel hot path on GB300.
+
+Workload (default): a Llama-2-7B-shaped bf16 gradient bucket (6,738,415,616
+elements), 4-bit codes, block 256, W = 8 simulated ranks held as 8 packed
+buffers in one HBM.  One step is one pass of the whole hot path:
+
+  loco_compress      rank 0's bucket: compensate, quantise, pack, error update
+  loco_decode_reduce the 8 ranks' packed buckets -> fp32 mean
+  loco_adam_step     the same 8 buffers decoded, averaged and fed to Adam(W)
+
+Ranks 1..7's packed buffers are produced before timing by compressing their
+own seeded gradients.  Inputs (176 GB live) are far larger than L2, so no L2
+flush is needed between steps.
+
+value = gradient bytes processed per second: compress counts N*2 bytes (bf16
+gradient), decode-reduce and the fused Adam each count W*N*2 bytes (the
+gradient-equivalent of the W contributions they consume).  Each kernel's
+roofline fraction is algorithmic HBM bytes / its CUDA-event time / the
+measured HBM copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl loco|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step on a one-GPU-per-process box); value sums the
+ranks' units over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "compress & decode-reduce GB/s of gradient processed; % of GB300 HBM roofline"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="loco", choices=["loco", "reference"])
+    ap.add_argument("--workload", default="llama2-7b",
+                    help="llama2-7b (default), tinyllama, mixtral, or flat:<log2 n> (bf16, 4-bit, block 256, W 8)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- workload
+
+def workload(name: str):
+    from bit_gradient_compression_gb300 import workloads as wl
+    if name == "llama2-7b":
+        return wl.LLAMA2_7B
+    if name == "tinyllama":
+        return wl.TINYLLAMA
+    if name == "mixtral":
+        return wl.MIXTRAL_MOE
+    if name.startswith("flat:"):
+        import torch
+        n = 1 << int(name.split(":")[1])
+        return wl.Workload(f"flat-bf16-2^{name.split(':')[1]}", n, torch.bfloat16, 4, 256, 8, 1, "flat")
+    raise SystemExit(f"unknown workload {name}")
+
+
+def kernel_bytes(n, gsize, bits, block, W):
+    nb = -(-n // block)
+    cb = nb * block * bits // 8
+    sb = nb * 4
+    return {
+        "compress": n * gsize + 8 * n + cb + sb,
+        "decode_reduce": W * (cb + sb) + 4 * n,
+        "adam": W * (cb + sb) + 24 * n,
+    }
+
+
+def grad_units(n, gsize, W):
+    return {"compress": n * gsize, "decode_reduce": W * n * gsize, "adam": W * n * gsize}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_gradient_compression_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, units: int, n_elems: int):
+    """DRAM bytes per launch from the committed ncu summary, scaled by elements;
+    None when the kernels changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != source_hash() or kernel not in d.get("kernels", {}):
+        return None
+    k = d["kernels"][kernel]
+    return k["dram_bytes_per_element"] * n_elems
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", self.gpu_id],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        busy = [s for s, p in zip(sm, power) if p > 0] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def host_mem_available():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except Exception:
+        return None
+    return None
+
+
+def gpu_uuid(dev) -> str:
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        return "GPU-" + str(u)
+    except Exception:
+        return str(dev.index or 0)
+
+
+# ----------------------------------------------------------------------------- CPU oracle (baseline)
+
+def prefix_layout(layout, count):
+    out, tot = [], 0
+    for name, n in layout:
+        if tot >= count:
+            break
+        take_n = min(n, count - tot)
+        out.append((name, take_n))
+        tot += take_n
+    return out
+
+
+def oracle_sample(w, S, seed=7):
+    """Host inputs for an S-element prefix of the workload: rank 0's gradient,
+    the error, W ranks' packed buffers (ranks 1.. compressed by the oracle,
+    untimed), parameters and Adam state."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from bit_gradient_compression_gb300 import workloads as wl
+
+    def grad(r):
+        t = torch.empty(S, dtype=w.grad_dtype)
+        if w.kind == "llm":
+            lay = prefix_layout(w.layout, S)
+            sig_rng = np.random.default_rng(wl.seed_for(seed, 1, r))
+            sig = 10.0 ** sig_rng.uniform(-5.0, -2.0, size=len(w.layout))[:len(lay)]
+            gen = torch.Generator().manual_seed(wl.seed_for(seed, 1, r))
+            off = 0
+            for (nm, n), s in zip(lay, sig):
+                t[off:off + n].copy_(torch.randn(n, generator=gen) * float(s))
+                off += n
+        else:
+            w.fill(t, wl.seed_for(seed, 1, r))
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16).copy()
+        return t.numpy().copy()
+
+    codes, scales = [], []
+    for r in range(1, w.W):
+        c, s = oracle.compress(grad(r), np.zeros(S, np.float32), 1, bits=w.bits, block=w.block, beta=0.9,
+                               kappa=4.0, threads=os.cpu_count() or 1)
+        codes.append(c)
+        scales.append(s)
+    g0 = grad(0)
+    e = np.zeros(S, np.float32)
+    rng = np.random.default_rng(3)
+    p = rng.uniform(-0.02, 0.02, S).astype(np.float32)
+    return g0, e, codes, scales, p, np.zeros(S, np.float32), np.zeros(S, np.float32)
+
+
+def oracle_step(w, S, inp, step, threads):
+    import oracle
+    g0, e, codes, scales, p, m, v = inp
+    c0, s0 = oracle.compress(g0, e, step, bits=w.bits, block=w.block, beta=0.9, kappa=4.0, reset_period=512,
+                             threads=threads)
+    allc, alls = [c0] + codes, [s0] + scales
+    oracle.decode_reduce(allc, alls, S, bits=w.bits, block=w.block, threads=threads)
+    oracle.adam_step(allc, alls, S, p, m, v, step, bits=w.bits, block=w.block, lr=1e-4, beta1=0.9, beta2=0.95,
+                     eps=1e-8, threads=threads)
+
+
+def cpu_baseline(w, S, steps, warmup):
+    """Times the oracle, as it stands, on all host cores over an S-element sample."""
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    inp = oracle_sample(w, S)
+    gsize = 2 if "bf16" in str(w.grad_dtype) else 4
+    for k in range(warmup):
+        oracle_step(w, S, inp, k + 1, threads)
+    t0 = time.perf_counter()
+    for k in range(steps):
+        oracle_step(w, S, inp, warmup + k + 1, threads)
+    dt = (time.perf_counter() - t0) / steps
+    units = sum(grad_units(S, gsize, w.W).values())
+    return {"value": units / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {S:,} elements of the {w.name} bucket (rank 0 compress + decode-reduce + Adam over "
+                      f"W={w.W} ranks), {steps} timed step(s) after {warmup} warm-up, same gradient law on host",
+            "ms_per_step": dt * 1e3}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_loco(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from bit_gradient_compression_gb300 import loco as L
+    from bit_gradient_compression_gb300 import workloads as wl
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args.workload)
+    n, bits, block, W = w.n, w.bits, w.block, w.W
+    gsize = 2 if w.grad_dtype == torch.bfloat16 else 4
+    cfg = L.make_config(bits=bits, block=block, beta=0.9, err_scale_mult=4.0, reset_period=512)
+    hp = L.make_adam(lr=1e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+
+    # ---- resident buffers (setup, untimed)
+    g = torch.empty(n, dtype=w.grad_dtype, device=dev)
+    e = torch.zeros(n, dtype=torch.float32, device=dev)
+    codes = [torch.empty(cb, dtype=torch.uint8, device=dev) for _ in range(W)]
+    scales = [torch.empty(nb, dtype=torch.float32, device=dev) for _ in range(W)]
+    for r in range(1, W):
+        w.fill(g, wl.seed_for(7, 1, r))
+        e.zero_()
+        L.loco_compress(cfg, g, e, 1, codes[r], scales[r])
+    w.fill(g, wl.seed_for(7, 1, 0))
+    e.zero_()
+    mean = torch.empty(n, dtype=torch.float32, device=dev)
+    param = wl.fill_uniform(torch.empty(n, device=dev), 3, -0.02, 0.02)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    step_no = [0]
+
+    def one_step(ev=None):
+        step_no[0] += 1
+        k = step_no[0]
+        if ev:
+            ev[0].record(stream)
+        L.loco_compress(cfg, g, e, k, codes[0], scales[0])
+        if ev:
+            ev[1].record(stream)
+        L.loco_decode_reduce(cfg, codes, scales, n, mean)
+        if ev:
+            ev[2].record(stream)
+        L.loco_adam_step(cfg, codes, scales, n, param, m, v, hp, k)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(gpu_uuid(dev)) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        one_step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    total_ms = t_start.elapsed_time(t_end)
+    per_kernel = {
+        "compress": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
+        "decode_reduce": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
+        "adam": statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs),
+    }
+
+    # ---- e2e: host buffers in page-locked memory, copies inside the timed region
+    e2e = None
+    h2d = n * gsize + (W - 1) * (cb + 4 * nb)
+    d2h = cb + 4 * nb
+    need = h2d + d2h
+    avail = host_mem_available()
+    e2e_skip = None
+    if args.e2e_steps <= 0:
+        e2e_skip = "disabled"
+    elif avail is not None and need > 0.6 * avail:
+        e2e_skip = f"host buffers need {need / 1e9:.1f} GB, only {avail / 1e9:.1f} GB available"
+    if e2e_skip is None:
+        hosts = []
+
+        def host_like(t):
+            h = torch.empty(t.numel(), dtype=t.dtype)
+            rc = torch.cuda.cudart().cudaHostRegister(h.data_ptr(), h.numel() * h.element_size(), 0)
+            if int(rc) != 0:
+                raise RuntimeError(f"cudaHostRegister failed ({rc})")
+            hosts.append(h)
+            return h
+
+        g_h = host_like(g)
+        g_h.copy_(g)
+        codes_h = [host_like(codes[r]) for r in range(1, W)]
+        scales_h = [host_like(scales[r]) for r in range(1, W)]
+        for r in range(1, W):
+            codes_h[r - 1].copy_(codes[r])
+            scales_h[r - 1].copy_(scales[r])
+        out_c = host_like(codes[0])
+        out_s = host_like(scales[0])
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            g.copy_(g_h, non_blocking=True)
+            for r in range(1, W):
+                codes[r].copy_(codes_h[r - 1], non_blocking=True)
+                scales[r].copy_(scales_h[r - 1], non_blocking=True)
+            one_step()
+            out_c.copy_(codes[0], non_blocking=True)
+            out_s.copy_(scales[0], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e = (a.elapsed_time(b) / args.e2e_steps, h2d, d2h)
+        for h in hosts:
+            torch.cuda.cudart().cudaHostUnregister(h.data_ptr())
+        del hosts, g_h, codes_h, scales_h, out_c, out_s
+
+    units_step = sum(grad_units(n, gsize, W).values())
+    t_ms = total_ms / args.steps
+    if world > 1:
+        tt = torch.tensor([t_ms, e2e[0] if e2e else 0.0], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms, e2e_max = float(tt[0]), float(tt[1])
+        if e2e:
+            e2e = (e2e_max, e2e[1], e2e[2])
+    if rank != 0:
+        return None
+
+    hbm, hbm_kind = peaks()
+    kb = kernel_bytes(n, gsize, bits, block, W)
+    roof = {}
+    for k, ms in per_kernel.items():
+        ach = kb[k] / (ms * 1e-3) / 1e9
+        roof[k] = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                   "frac": round(ach / hbm, 4), "ms": round(ms, 4),
+                   "traffic": ncu_traffic(k, kb[k], n), "algorithmic_bytes": kb[k],
+                   "grad_GBps": round(grad_units(n, gsize, W)[k] / (ms * 1e-3) / 1e9, 1),
+                   "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured" else
+                   "fallback"}
+    dominant = max(per_kernel, key=per_kernel.get)
+    value = world * units_step / (t_ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "n_elements": n, "grad_dtype": "bf16" if gsize == 2 else "fp32",
+                   "bits": bits, "block": block, "W": W, "beta": 0.9, "kappa": 4.0,
+                   "step": "loco_compress(rank 0) + loco_decode_reduce(W) + loco_adam_step(W)",
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU, W ranks simulated in HBM"},
+        "roofline": dict(roof[dominant], kernel=dominant),
+        "roofline_kernels": roof,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if e2e_skip:
+        out["e2e"] = {"value": None, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "skipped": e2e_skip}
+    if e2e:
+        e2e_ms, h2d, d2h = e2e
+        out["e2e"] = {"value": round(world * units_step / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                      "what": "pinned host -> device: rank 0 gradient + ranks 1..W-1 packed buffers; "
+                              "device -> pinned host: rank 0's packed buffer"}
+    return out
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        w = workload(args.workload)
+        S = min(w.n, 1 << 25)
+        cb = cpu_baseline(w, S, args.steps, args.warmup)
+        out = {"impl": "reference", "metric": METRIC, "value": round(cb["value"], 3), "unit": UNIT,
+               "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": round(cb["ms_per_step"], 3), "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+               "config": {"workload": w.name, "n_elements": w.n, "sample_elements": S, "bits": w.bits,
+                          "block": w.block, "W": w.W},
+               "cpu_baseline": cb,
+               "e2e": {"value": round(cb["value"], 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+               "note": "the reference arm is the CPU oracle (plain C, fp32) timed on the host cores"}
+        print(json.dumps(out), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    out = run_loco(args, rank, world)
+    if rank == 0:
+        w = workload(args.workload)
+        S = min(w.n, 1 << 27)
+        try:
+            out["cpu_baseline"] = cpu_baseline(w, S, 1, 1)
+        except Exception as ex:  # the GPU numbers stand without it
+            out["cpu_baseline"] = {"value": None, "error": repr(ex)}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

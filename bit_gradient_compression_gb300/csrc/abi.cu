@@ -1,0 +1,313 @@
+// C ABI of libloco (declared in include/loco.h): argument validation,
+// derived constants, and dispatch to the kernel launchers.
+//
+// Every check happens on the host before anything is launched, so a rejected
+// call writes nothing.  Device buffers are checked against the extent of the
+// allocation they live in (cuMemGetAddressRange, fetched through the runtime's
+// driver entry point so the library has no link-time dependency on libcuda):
+// a host pointer, a pointer of another device or a buffer shorter than the
+// call needs is an argument error, not a memory fault.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "loco.h"
+#include "loco_internal.h"
+
+namespace loco {
+
+static thread_local char g_last_error[512] = "";
+
+static loco_status fail(loco_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+int persistent_grid(const void* kernel, int threads) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+  if (sms <= 0) sms = 1;
+  if (per_sm <= 0) per_sm = 1;
+  return sms * per_sm;
+}
+
+typedef CUresult (*AddressRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+static AddressRangeFn address_range_fn() {
+  static AddressRangeFn fn = []() -> AddressRangeFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<AddressRangeFn>(p);
+  }();
+  return fn;
+}
+
+// Null and alignment check (no CUDA call).
+static loco_status check_ptr(const void* p, size_t align, const char* name) {
+  if (p == nullptr) return fail(LOCO_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) % align != 0)
+    return fail(LOCO_ERR_MISALIGNED, "%s (%p) is not %zu-byte aligned", name, p, align);
+  return LOCO_OK;
+}
+
+// Checks that [p, p + bytes) is device memory of the current device inside one
+// allocation.  name is used in the error text.
+static loco_status check_extent(const void* p, size_t bytes, const char* name) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(LOCO_ERR_INVALID_ARG, "%s: cudaPointerGetAttributes failed: %s", name, cudaGetErrorString(e));
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(LOCO_ERR_INVALID_ARG, "%s (%p) is not device memory", name, p);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (attr.type == cudaMemoryTypeDevice && attr.device != dev)
+    return fail(LOCO_ERR_INVALID_ARG, "%s lives on device %d but device %d is current", name, attr.device, dev);
+  AddressRangeFn range = address_range_fn();
+  if (range != nullptr) {
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) == CUDA_SUCCESS) {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+      if (lo + bytes > uintptr_t(base) + size)
+        return fail(LOCO_ERR_INVALID_ARG, "%s: %zu bytes from %p run past the end of its allocation (%zu bytes at %p)",
+                    name, bytes, p, size, reinterpret_cast<void*>(base));
+    }
+  }
+  return LOCO_OK;
+}
+
+// A list of buffers checked together: every null/alignment rule first, then
+// the device-memory and extent rules, so the status does not depend on which
+// buffer happens to be listed first.
+struct BufCheck {
+  const void* p;
+  size_t bytes;
+  size_t align;
+  const char* name;
+};
+
+static loco_status check_buffers(const BufCheck* b, int count) {
+  for (int i = 0; i < count; ++i) {
+    loco_status st = check_ptr(b[i].p, b[i].align, b[i].name);
+    if (st != LOCO_OK) return st;
+  }
+  for (int i = 0; i < count; ++i) {
+    loco_status st = check_extent(b[i].p, b[i].bytes, b[i].name);
+    if (st != LOCO_OK) return st;
+  }
+  return LOCO_OK;
+}
+
+static bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+static loco_status check_layout(int32_t bits, int32_t block) {
+  if (bits != 4 && bits != 8) return fail(LOCO_ERR_UNSUPPORTED, "bits = %d (supported: 4, 8)", bits);
+  if (block != 64 && block != 128 && block != 256)
+    return fail(LOCO_ERR_UNSUPPORTED, "block = %d (supported: 64, 128, 256)", block);
+  return LOCO_OK;
+}
+
+static loco_status launch_result(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(LOCO_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+  g_last_error[0] = '\0';
+  return LOCO_OK;
+}
+
+static loco_status check_ranks(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales,
+                               int32_t W, int64_t n, RankPtrs* out, BufCheck* list, int* count) {
+  if (codes == nullptr || scales == nullptr) return fail(LOCO_ERR_INVALID_ARG, "codes or scales array is NULL");
+  static thread_local char names[2 * kMaxRanks][16];
+  const size_t cbytes = size_t(loco_code_bytes(n, cfg->bits, cfg->block));
+  const size_t sbytes = size_t(loco_num_blocks(n, cfg->block)) * sizeof(float);
+  for (int w = 0; w < W; ++w) {
+    snprintf(names[2 * w], 16, "codes[%d]", w);
+    snprintf(names[2 * w + 1], 16, "scales[%d]", w);
+    list[(*count)++] = BufCheck{codes[w], cbytes, 16, names[2 * w]};
+    list[(*count)++] = BufCheck{scales[w], sbytes, 4, names[2 * w + 1]};
+    out->codes[w] = codes[w];
+    out->scales[w] = scales[w];
+  }
+  for (int w = W; w < kMaxRanks; ++w) {
+    out->codes[w] = nullptr;
+    out->scales[w] = nullptr;
+  }
+  return LOCO_OK;
+}
+
+}  // namespace loco
+
+using namespace loco;
+
+extern "C" {
+
+int64_t loco_num_blocks(int64_t n, int32_t block) {
+  if (n <= 0 || block <= 0) return 0;
+  return (n + block - 1) / block;
+}
+
+int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block) {
+  if (n <= 0 || block <= 0 || bits <= 0) return 0;
+  return loco_num_blocks(n, block) * block * bits / 8;
+}
+
+const char* loco_status_string(loco_status s) {
+  switch (s) {
+    case LOCO_OK: return "LOCO_OK";
+    case LOCO_ERR_INVALID_ARG: return "LOCO_ERR_INVALID_ARG";
+    case LOCO_ERR_UNSUPPORTED: return "LOCO_ERR_UNSUPPORTED";
+    case LOCO_ERR_MISALIGNED: return "LOCO_ERR_MISALIGNED";
+    case LOCO_ERR_CUDA: return "LOCO_ERR_CUDA";
+  }
+  return "LOCO_ERR_UNKNOWN";
+}
+
+const char* loco_last_error(void) { return g_last_error; }
+
+loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad_dtype, float* err, int64_t n,
+                          int64_t step, uint8_t* codes, float* scales, loco_stream_t stream) {
+  if (cfg == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg is NULL");
+  loco_status st = check_layout(cfg->bits, cfg->block);
+  if (st != LOCO_OK) return st;
+  if (grad_dtype != LOCO_F32 && grad_dtype != LOCO_BF16)
+    return fail(LOCO_ERR_UNSUPPORTED, "grad_dtype = %d (LOCO_F32 or LOCO_BF16)", grad_dtype);
+  if (cfg->scale_mode != LOCO_SCALE_ABSMAX && cfg->scale_mode != LOCO_SCALE_FIXED)
+    return fail(LOCO_ERR_UNSUPPORTED, "scale_mode = %d", cfg->scale_mode);
+  if (!(cfg->beta >= 0.0f && cfg->beta <= 1.0f)) return fail(LOCO_ERR_INVALID_ARG, "beta = %g not in [0, 1]", cfg->beta);
+  if (!(cfg->err_scale_mult > 0.0f) || !isfinite(cfg->err_scale_mult))
+    return fail(LOCO_ERR_INVALID_ARG, "err_scale_mult (kappa) = %g must be finite and > 0", cfg->err_scale_mult);
+  if (cfg->scale_mode == LOCO_SCALE_FIXED && (!(cfg->fixed_scale > 0.0f) || !isfinite(cfg->fixed_scale)))
+    return fail(LOCO_ERR_INVALID_ARG, "fixed_scale = %g must be finite and > 0", cfg->fixed_scale);
+  if (cfg->reset_period < 0) return fail(LOCO_ERR_INVALID_ARG, "reset_period = %lld < 0", (long long)cfg->reset_period);
+  if (n < 0) return fail(LOCO_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
+  if (step < 1) return fail(LOCO_ERR_INVALID_ARG, "step = %lld (1-based)", (long long)step);
+  if (n == 0) return LOCO_OK;
+
+  const size_t gbytes = size_t(n) * (grad_dtype == LOCO_BF16 ? 2 : 4);
+  const size_t ebytes = size_t(n) * 4;
+  const size_t cbytes = size_t(loco_code_bytes(n, cfg->bits, cfg->block));
+  const size_t sbytes = size_t(loco_num_blocks(n, cfg->block)) * 4;
+  const BufCheck bufs[4] = {{grad, gbytes, 16, "grad"}, {err, ebytes, 16, "err"}, {codes, cbytes, 16, "codes"},
+                            {scales, sbytes, 4, "scales"}};
+  if ((st = check_buffers(bufs, 4)) != LOCO_OK) return st;
+  if (overlap(grad, gbytes, err, ebytes) || overlap(grad, gbytes, codes, cbytes) || overlap(grad, gbytes, scales, sbytes) ||
+      overlap(err, ebytes, codes, cbytes) || overlap(err, ebytes, scales, sbytes) || overlap(codes, cbytes, scales, sbytes))
+    return fail(LOCO_ERR_INVALID_ARG, "grad, err, codes and scales must not overlap");
+
+  CompressArgs a;
+  a.grad = grad;
+  a.err = err;
+  a.codes = codes;
+  a.scales = scales;
+  a.n = n;
+  a.bits = cfg->bits;
+  a.block = cfg->block;
+  a.grad_bf16 = grad_dtype == LOCO_BF16;
+  a.fixed = cfg->scale_mode == LOCO_SCALE_FIXED;
+  a.fixed_delta = a.fixed ? 1.0f / cfg->fixed_scale : 0.0f;
+  a.fixed_inv = a.fixed ? cfg->fixed_scale : 0.0f;
+  a.beta = cfg->beta;
+  a.one_minus_beta = 1.0f - cfg->beta;
+  a.kappa = cfg->err_scale_mult;
+  a.reset = cfg->reset_period > 0 && (step % cfg->reset_period) == 0;
+  return launch_result(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)), "loco_compress");
+}
+
+loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales,
+                               int32_t W, int64_t n, float* mean, loco_stream_t stream) {
+  if (cfg == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg is NULL");
+  loco_status st = check_layout(cfg->bits, cfg->block);
+  if (st != LOCO_OK) return st;
+  if (n < 0) return fail(LOCO_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
+  if (W < 1) return fail(LOCO_ERR_INVALID_ARG, "W = %d (need >= 1)", W);
+  if (W > kMaxRanks) return fail(LOCO_ERR_UNSUPPORTED, "W = %d (at most %d)", W, kMaxRanks);
+  if (n == 0) return LOCO_OK;
+  ReduceArgs a;
+  BufCheck bufs[2 * kMaxRanks + 1];
+  int nbuf = 0;
+  if ((st = check_ranks(cfg, codes, scales, W, n, &a.ranks, bufs, &nbuf)) != LOCO_OK) return st;
+  const size_t mbytes = size_t(n) * 4;
+  bufs[nbuf++] = BufCheck{mean, mbytes, 16, "mean"};
+  if ((st = check_buffers(bufs, nbuf)) != LOCO_OK) return st;
+  const size_t cbytes = size_t(loco_code_bytes(n, cfg->bits, cfg->block));
+  const size_t sbytes = size_t(loco_num_blocks(n, cfg->block)) * 4;
+  for (int w = 0; w < W; ++w)
+    if (overlap(mean, mbytes, codes[w], cbytes) || overlap(mean, mbytes, scales[w], sbytes))
+      return fail(LOCO_ERR_INVALID_ARG, "mean overlaps the inputs of rank %d", w);
+  a.W = W;
+  a.n = n;
+  a.bits = cfg->bits;
+  a.block = cfg->block;
+  a.mean = mean;
+  return launch_result(launch_decode_reduce(a, reinterpret_cast<cudaStream_t>(stream)), "loco_decode_reduce");
+}
+
+loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales, int32_t W,
+                           int64_t n, float* param, float* m, float* v, const loco_adam_hparams* hp, int64_t t,
+                           loco_stream_t stream) {
+  if (cfg == nullptr || hp == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg or hp is NULL");
+  loco_status st = check_layout(cfg->bits, cfg->block);
+  if (st != LOCO_OK) return st;
+  if (n < 0) return fail(LOCO_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
+  if (W < 1) return fail(LOCO_ERR_INVALID_ARG, "W = %d (need >= 1)", W);
+  if (W > kMaxRanks) return fail(LOCO_ERR_UNSUPPORTED, "W = %d (at most %d)", W, kMaxRanks);
+  if (t < 1) return fail(LOCO_ERR_INVALID_ARG, "t = %lld (1-based)", (long long)t);
+  if (!isfinite(hp->lr) || !isfinite(hp->eps) || !isfinite(hp->weight_decay) || hp->eps < 0.0f)
+    return fail(LOCO_ERR_INVALID_ARG, "lr, eps, weight_decay must be finite and eps >= 0");
+  if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+    return fail(LOCO_ERR_INVALID_ARG, "beta1 = %g, beta2 = %g must lie in [0, 1)", hp->beta1, hp->beta2);
+  if (n == 0) return LOCO_OK;
+  AdamArgs a;
+  BufCheck bufs[2 * kMaxRanks + 3];
+  int nbuf = 0;
+  if ((st = check_ranks(cfg, codes, scales, W, n, &a.ranks, bufs, &nbuf)) != LOCO_OK) return st;
+  const size_t fbytes = size_t(n) * 4;
+  bufs[nbuf++] = BufCheck{param, fbytes, 16, "param"};
+  bufs[nbuf++] = BufCheck{m, fbytes, 16, "m"};
+  bufs[nbuf++] = BufCheck{v, fbytes, 16, "v"};
+  if ((st = check_buffers(bufs, nbuf)) != LOCO_OK) return st;
+  if (overlap(param, fbytes, m, fbytes) || overlap(param, fbytes, v, fbytes) || overlap(m, fbytes, v, fbytes))
+    return fail(LOCO_ERR_INVALID_ARG, "param, m and v must not overlap");
+  const size_t cbytes = size_t(loco_code_bytes(n, cfg->bits, cfg->block));
+  const size_t sbytes = size_t(loco_num_blocks(n, cfg->block)) * 4;
+  for (int w = 0; w < W; ++w)
+    for (const float* out : {static_cast<const float*>(param), static_cast<const float*>(m), static_cast<const float*>(v)})
+      if (overlap(out, fbytes, codes[w], cbytes) || overlap(out, fbytes, scales[w], sbytes))
+        return fail(LOCO_ERR_INVALID_ARG, "param/m/v overlap the inputs of rank %d", w);
+  a.W = W;
+  a.n = n;
+  a.bits = cfg->bits;
+  a.block = cfg->block;
+  a.param = param;
+  a.m = m;
+  a.v = v;
+  a.lr = hp->lr;
+  a.beta1 = hp->beta1;
+  a.beta2 = hp->beta2;
+  a.one_minus_beta1 = 1.0f - hp->beta1;
+  a.one_minus_beta2 = 1.0f - hp->beta2;
+  a.lr_wd = hp->lr * hp->weight_decay;
+  a.bc1 = hp->bias_correction ? float(1.0 - pow(double(hp->beta1), double(t))) : 1.0f;
+  a.bc2 = hp->bias_correction ? float(1.0 - pow(double(hp->beta2), double(t))) : 1.0f;
+  a.eps = hp->eps;
+  a.eps_inside_sqrt = hp->eps_inside_sqrt != 0;
+  return launch_result(launch_adam(a, reinterpret_cast<cudaStream_t>(stream)), "loco_adam_step");
+}
+
+}  // extern "C"

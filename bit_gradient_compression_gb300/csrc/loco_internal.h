@@ -1,0 +1,70 @@
+// Internal interface between the C ABI (abi.cu) and the kernel launchers.
+// Not installed; the public interface is include/loco.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace loco {
+
+constexpr int kMaxRanks = 16;
+
+// Everything the sender kernel needs, resolved on the host.
+struct CompressArgs {
+  const void* grad;
+  float* err;
+  uint8_t* codes;
+  float* scales;
+  int64_t n;
+  int bits;
+  int block;
+  int grad_bf16;
+  int fixed;          // 1: one fixed step for every block
+  float fixed_delta;  // 1/s (host fp32 division)
+  float fixed_inv;    // s
+  float beta;
+  float one_minus_beta;  // 1 - beta, formed once in fp32
+  float kappa;
+  int reset;          // this step zeroes the stored error
+};
+
+struct RankPtrs {
+  const uint8_t* codes[kMaxRanks];
+  const float* scales[kMaxRanks];
+};
+
+struct ReduceArgs {
+  RankPtrs ranks;
+  int W;
+  int64_t n;
+  int bits;
+  int block;
+  float* mean;
+};
+
+struct AdamArgs {
+  RankPtrs ranks;
+  int W;
+  int64_t n;
+  int bits;
+  int block;
+  float* param;
+  float* m;
+  float* v;
+  float lr;
+  float beta1, beta2;
+  float one_minus_beta1, one_minus_beta2;
+  float lr_wd;
+  float bc1, bc2;
+  float eps;
+  int eps_inside_sqrt;
+};
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
+cudaError_t launch_decode_reduce(const ReduceArgs& a, cudaStream_t s);
+cudaError_t launch_adam(const AdamArgs& a, cudaStream_t s);
+
+// Number of CTAs for a grid-stride kernel: resident CTAs per SM x SMs.
+int persistent_grid(const void* kernel, int threads);
+
+}  // namespace loco

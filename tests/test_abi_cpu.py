@@ -1,0 +1,110 @@
+"""libloco without a GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_gradient_compression_gb300 import build
+    build.build()
+    from bit_gradient_compression_gb300 import loco
+    return loco
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "loco.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(loco_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert len(names) >= 7
+    raw = ctypes.CDLL(L.LIB_PATH)
+    for name in names:
+        assert hasattr(raw, name), name
+    assert set(names) == set(L.EXPORTS)
+
+
+def test_sizes(L):
+    assert L.loco_num_blocks(0, 256) == 0
+    assert L.loco_num_blocks(1, 256) == 1
+    assert L.loco_num_blocks(257, 256) == 2
+    assert L.loco_code_bytes(257, 4, 256) == 256
+    assert L.loco_code_bytes(257, 8, 64) == 5 * 64
+    n7b = 6_738_415_616
+    assert L.loco_num_blocks(n7b, 256) == 26_321_936
+    assert L.loco_code_bytes(n7b, 4, 256) == n7b // 2
+    assert L.loco_code_bytes(1 << 31, 8, 64) == 1 << 31
+
+
+def _compress(L, cfg, **kw):
+    a = dict(grad=0x10000, err=0x20000, step=1, codes=0x30000, scales=0x40000, n=1000, grad_dtype=0, stream=0)
+    a.update(kw)
+    return L.loco_compress(cfg, a["grad"], a["err"], a["step"], a["codes"], a["scales"], n=a["n"],
+                           grad_dtype=a["grad_dtype"], stream=a["stream"])
+
+
+def _status(L, fn):
+    try:
+        fn()
+    except L.LocoError as e:
+        return e.status
+    return L.LOCO_OK
+
+
+def test_argument_errors(L):
+    ok = L.make_config()
+    st = lambda **kw: _status(L, lambda: _compress(L, kw.pop("cfg", ok), **kw))
+    assert st(cfg=L.make_config(bits=3)) == L.LOCO_ERR_UNSUPPORTED
+    assert st(cfg=L.make_config(block=32)) == L.LOCO_ERR_UNSUPPORTED
+    assert st(cfg=L.make_config(block=512)) == L.LOCO_ERR_UNSUPPORTED
+    assert st(grad_dtype=7) == L.LOCO_ERR_UNSUPPORTED
+    assert st(cfg=L.make_config(beta=1.5)) == L.LOCO_ERR_INVALID_ARG
+    assert st(cfg=L.make_config(beta=-0.1)) == L.LOCO_ERR_INVALID_ARG
+    assert st(cfg=L.make_config(beta=float("nan"))) == L.LOCO_ERR_INVALID_ARG
+    assert st(cfg=L.make_config(err_scale_mult=0.0)) == L.LOCO_ERR_INVALID_ARG
+    assert st(cfg=L.make_config(fixed_scale=-1.0)) == L.LOCO_ERR_INVALID_ARG
+    assert st(cfg=L.make_config(reset_period=-1)) == L.LOCO_ERR_INVALID_ARG
+    assert st(n=-1) == L.LOCO_ERR_INVALID_ARG
+    assert st(step=0) == L.LOCO_ERR_INVALID_ARG
+    assert st(grad=0) == L.LOCO_ERR_INVALID_ARG
+    assert st(err=0) == L.LOCO_ERR_INVALID_ARG
+    assert st(grad=0x10001) == L.LOCO_ERR_MISALIGNED
+    assert st(codes=0x30008) == L.LOCO_ERR_MISALIGNED
+    assert st(scales=0x40002) == L.LOCO_ERR_MISALIGNED
+    # n == 0 is an empty, successful call (nothing is launched or dereferenced)
+    assert st(n=0, grad=0, err=0, codes=0, scales=0) == L.LOCO_OK
+    # non-device memory is refused before any launch (here: no driver at all)
+    assert st() == L.LOCO_ERR_INVALID_ARG
+    assert L.lib.loco_last_error().decode() != ""
+
+
+def test_rank_argument_errors(L):
+    cfg = L.make_config()
+    hp = L.make_adam()
+    dr = lambda W, n=100: _status(L, lambda: L.loco_decode_reduce(cfg, [0x1000] * W, [0x2000] * W, n, 0x3000, stream=0))
+    assert dr(0) == L.LOCO_ERR_INVALID_ARG
+    assert dr(17) == L.LOCO_ERR_UNSUPPORTED
+    assert dr(4, n=-5) == L.LOCO_ERR_INVALID_ARG
+    assert dr(4, n=0) == L.LOCO_OK
+    assert _status(L, lambda: L.loco_decode_reduce(cfg, [0x1001], [0x2000], 10, 0x3000, stream=0)) == L.LOCO_ERR_MISALIGNED
+    ad = lambda W, t=1, hp=hp: _status(L, lambda: L.loco_adam_step(cfg, [0x1000] * W, [0x2000] * W, 100, 0x3000,
+                                                                  0x4000, 0x5000, hp, t, stream=0))
+    assert ad(0) == L.LOCO_ERR_INVALID_ARG
+    assert ad(17) == L.LOCO_ERR_UNSUPPORTED
+    assert ad(2, t=0) == L.LOCO_ERR_INVALID_ARG
+    assert ad(2, hp=L.make_adam(beta1=1.0)) == L.LOCO_ERR_INVALID_ARG
+    assert ad(2, hp=L.make_adam(eps=-1.0)) == L.LOCO_ERR_INVALID_ARG
+    assert ad(2, hp=L.make_adam(lr=float("inf"))) == L.LOCO_ERR_INVALID_ARG
+
+
+def test_status_strings(L):
+    for s in range(5):
+        assert L.lib.loco_status_string(s).decode().startswith("LOCO_")

@@ -1,0 +1,266 @@
+"""CUDA path vs. CPU oracle, element by element, through the C ABI.
+
+Small and medium buckets (several blocks, ragged tails, every bits/block/dtype
+combination, W = 1..16) are compared in full; guard bytes around every output
+buffer must survive each call.  The bar is bit-exact: codes and scales are
+integer/byte results, and the fp32 error, mean and Adam state are computed in
+the same operation order on both sides.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.helpers import assert_bits_equal, grad_to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+CANARY = 0xA5
+GUARD = 64
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_gradient_compression_gb300 import loco
+    torch.cuda.set_device(DEV)
+    return loco
+
+
+def wl():
+    from bit_gradient_compression_gb300 import workloads
+    return workloads
+
+
+class Guarded:
+    """A device buffer with GUARD canary bytes after the part a call may write."""
+
+    def __init__(self, nbytes: int, dtype=torch.uint8):
+        self.nbytes = nbytes
+        self.raw = torch.full((nbytes + GUARD,), CANARY, dtype=torch.uint8, device=DEV)
+        self.dtype = dtype
+
+    def view(self):
+        return self.raw[: self.nbytes].view(self.dtype)
+
+    def intact(self) -> bool:
+        return bool((self.raw[self.nbytes:] == CANARY).all())
+
+
+def _grad(n, dtype, seed, outliers=True):
+    g = torch.empty(n, dtype=dtype, device=DEV)
+    return wl().fill_flat_normal(g, seed, outlier_p=1e-2 if outliers else 0.0)
+
+
+SIZES = [1, 7, 8, 9, 63, 64, 65, 255, 257, 3 * 2048 + 5, 100_003, 1 << 16]
+
+
+def _compress_both(L, cfg_kw, n, dtype, steps, seed, fixed_scale=None, grad_fn=None):
+    bits, block = cfg_kw["bits"], cfg_kw["block"]
+    cfg = L.make_config(fixed_scale=fixed_scale, **cfg_kw)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    e = Guarded(4 * n, torch.float32)
+    e.view().zero_()
+    codes, scales = Guarded(cb), Guarded(4 * nb, torch.float32)
+    e_h = np.zeros(n, dtype=np.float32)
+    okw = dict(bits=bits, block=block, beta=cfg_kw["beta"], kappa=cfg_kw["err_scale_mult"],
+               reset_period=cfg_kw["reset_period"], fixed_scale=fixed_scale)
+    for step in range(1, steps + 1):
+        g = grad_fn(step) if grad_fn else _grad(n, dtype, seed + 1000 * step)
+        g_h = grad_to_np(g)
+        L.loco_compress(cfg, g, e.view(), step, codes.view(), scales.view())
+        oc, os_ = oracle.compress(g_h, e_h, step, **okw)
+        torch.cuda.synchronize()
+        tag = f"n={n} bits={bits} block={block} {dtype} step={step}"
+        assert_bits_equal(codes.view().cpu().numpy(), oc, "codes " + tag)
+        assert_bits_equal(scales.view().cpu().numpy(), os_, "scales " + tag)
+        assert_bits_equal(e.view().cpu().numpy(), e_h, "err " + tag)
+        assert e.intact() and codes.intact() and scales.intact(), "guard bytes overwritten " + tag
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("block", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_compress_parity_small(L, bits, block, dtype):
+    for i, n in enumerate(SIZES):
+        _compress_both(L, dict(bits=bits, block=block, beta=0.9, err_scale_mult=4.0, reset_period=2),
+                       n, dtype, 3, 100 * i + bits + block)
+
+
+@pytest.mark.parametrize("beta", [0.0, 0.5, 1.0, 0.37])
+@pytest.mark.parametrize("kappa", [4.0, 6.0])
+def test_compress_parity_beta_kappa(L, beta, kappa):
+    _compress_both(L, dict(bits=4, block=128, beta=beta, err_scale_mult=kappa, reset_period=3),
+                   50_001, torch.bfloat16, 4, 77)
+
+
+@pytest.mark.parametrize("s", [2.0 ** 19, 2.0 ** 17, 1000.0])
+@pytest.mark.parametrize("bits", [4, 8])
+def test_compress_parity_fixed_scale(L, s, bits):
+    _compress_both(L, dict(bits=bits, block=256, beta=0.9, err_scale_mult=6.0, reset_period=0),
+                   20_000 + 3, torch.float32, 3, 91, fixed_scale=s)
+
+
+def test_compress_zero_and_constant_blocks(L):
+    n, block = 64 * 40 + 17, 64
+
+    def gfn(step):
+        g = _grad(n, torch.float32, 5 + step)
+        g[128:512] = 0            # whole zero blocks
+        g[1024:1088] = 3.5e-3     # a constant block
+        g[2000:2064] = -7 * 2.0 ** -12
+        return g
+    _compress_both(L, dict(bits=4, block=block, beta=0.9, err_scale_mult=4.0, reset_period=0), n,
+                   torch.float32, 3, 0, grad_fn=gfn)
+
+
+def test_compress_nonfinite_stays_in_bounds(L):
+    """Non-finite input values are outside the contract, but the call must not
+    write outside its buffers; finite blocks must still match the oracle."""
+    n, bits, block = 4096 + 9, 4, 128
+    cfg = L.make_config(bits=bits, block=block)
+    g = _grad(n, torch.float32, 3)
+    g[130] = float("nan")
+    g[700] = float("inf")
+    g[1500] = -float("inf")
+    e = Guarded(4 * n, torch.float32)
+    e.view().zero_()
+    codes = Guarded(L.loco_code_bytes(n, bits, block))
+    scales = Guarded(4 * L.loco_num_blocks(n, block), torch.float32)
+    L.loco_compress(cfg, g, e.view(), 1, codes.view(), scales.view())
+    torch.cuda.synchronize()
+    assert e.intact() and codes.intact() and scales.intact()
+    e_h = np.zeros(n, dtype=np.float32)
+    oc, os_ = oracle.compress(grad_to_np(g), e_h, 1, bits=bits, block=block, beta=0.9, kappa=4.0)
+    finite_blocks = [b for b in range(L.loco_num_blocks(n, block)) if b not in (1, 5, 11)]
+    sc = scales.view().cpu().numpy()
+    for b in finite_blocks:
+        assert sc[b] == os_[b]
+
+
+def _random_ranks(L, n, bits, block, W, seed):
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(seed)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    codes = [torch.randint(0, 256, (cb,), dtype=torch.uint8, device=DEV, generator=gen) for _ in range(W)]
+    scales = []
+    for _ in range(W):
+        s = torch.rand(nb, device=DEV, generator=gen) * 1e-3
+        s[torch.rand(nb, device=DEV, generator=gen) < 0.05] = 0.0
+        scales.append(s)
+    return codes, scales
+
+
+DEC_SIZES = [1, 9, 255, 1000, (1 << 16) + 3]
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 7, 8, 9, 13, 16])
+@pytest.mark.parametrize("bits,block", [(4, 256), (4, 64), (8, 128), (8, 256)])
+def test_decode_reduce_parity(L, W, bits, block):
+    cfg = L.make_config(bits=bits, block=block)
+    for i, n in enumerate(DEC_SIZES):
+        codes, scales = _random_ranks(L, n, bits, block, W, 1000 * W + i)
+        mean = Guarded(4 * n, torch.float32)
+        L.loco_decode_reduce(cfg, codes, scales, n, mean.view())
+        om = oracle.decode_reduce([c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales], n,
+                                  bits=bits, block=block)
+        torch.cuda.synchronize()
+        assert_bits_equal(mean.view().cpu().numpy(), om, f"mean n={n} W={W}")
+        assert mean.intact()
+
+
+@pytest.mark.parametrize("W", [1, 3, 8, 16])
+@pytest.mark.parametrize("bits,block", [(4, 256), (8, 64)])
+@pytest.mark.parametrize("variant", ["adamw", "paper", "plain"])
+def test_adam_parity(L, W, bits, block, variant):
+    cfg = L.make_config(bits=bits, block=block)
+    if variant == "adamw":
+        hpk = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, bias_correction=True,
+                   eps_inside_sqrt=False)
+    elif variant == "paper":
+        hpk = dict(lr=3e-4, beta1=0.9, beta2=0.99, eps=1e-10, weight_decay=0.0, bias_correction=False,
+                   eps_inside_sqrt=True)
+    else:
+        hpk = dict(lr=1e-2, beta1=0.0, beta2=0.5, eps=1e-6, weight_decay=0.0, bias_correction=True,
+                   eps_inside_sqrt=False)
+    hp = L.make_adam(**hpk)
+    for i, n in enumerate([7, 1000, (1 << 16) + 5]):
+        p = wl().fill_uniform(torch.empty(n, device=DEV), i, -0.05, 0.05)
+        m = torch.zeros(n, device=DEV)
+        v = torch.zeros(n, device=DEV)
+        ph, mh, vh = p.cpu().numpy().copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+        for t in (1, 2, 3):
+            codes, scales = _random_ranks(L, n, bits, block, W, 7 * t + i)
+            L.loco_adam_step(cfg, codes, scales, n, p, m, v, hp, t)
+            oracle.adam_step([c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales], n, ph, mh, vh,
+                             t, bits=bits, block=block, **hpk)
+            torch.cuda.synchronize()
+            assert_bits_equal(p.cpu().numpy(), ph, f"param n={n} t={t}")
+            assert_bits_equal(m.cpu().numpy(), mh, f"m n={n} t={t}")
+            assert_bits_equal(v.cpu().numpy(), vh, f"v n={n} t={t}")
+
+
+def test_flat_1m_config_full(L):
+    """The 1M-element fp32 workload: 4 ranks, 8 steps, 4-bit, block 256,
+    beta 0.9 -- every rank's codes, scales and error, and the mean, compared in
+    full at every step."""
+    W_ = wl()
+    w = W_.FLAT_1M
+    n, bits, block, W = w.n, w.bits, w.block, w.W
+    cfg = L.make_config(bits=bits, block=block, beta=0.9, err_scale_mult=4.0, reset_period=512)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    errs = [torch.zeros(n, device=DEV) for _ in range(W)]
+    errs_h = [np.zeros(n, np.float32) for _ in range(W)]
+    codes = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    scales = [torch.empty(nb, device=DEV) for _ in range(W)]
+    mean = torch.empty(n, device=DEV)
+    for k in range(1, w.steps + 1):
+        oc_all, os_all = [], []
+        for r in range(W):
+            g = w.fill(torch.empty(n, dtype=w.grad_dtype, device=DEV), W_.seed_for(42, k, r))
+            L.loco_compress(cfg, g, errs[r], k, codes[r], scales[r])
+            oc, os_ = oracle.compress(grad_to_np(g), errs_h[r], k, bits=bits, block=block, beta=0.9, kappa=4.0,
+                                      reset_period=512, threads=8)
+            oc_all.append(oc)
+            os_all.append(os_)
+            torch.cuda.synchronize()
+            assert_bits_equal(codes[r].cpu().numpy(), oc, f"codes rank {r} step {k}")
+            assert_bits_equal(scales[r].cpu().numpy(), os_, f"scales rank {r} step {k}")
+            assert_bits_equal(errs[r].cpu().numpy(), errs_h[r], f"err rank {r} step {k}")
+        L.loco_decode_reduce(cfg, codes, scales, n, mean)
+        om = oracle.decode_reduce(oc_all, os_all, n, bits=bits, block=block, threads=8)
+        torch.cuda.synchronize()
+        mg = mean.cpu().numpy()
+        assert_bits_equal(mg, om, f"mean step {k}")
+
+
+def test_empty_and_errors(L):
+    cfg = L.make_config()
+    e = torch.empty(0, device=DEV)
+    L.loco_compress(cfg, torch.empty(0, device=DEV), e, 1, torch.empty(0, dtype=torch.uint8, device=DEV),
+                    torch.empty(0, device=DEV))
+    L.loco_decode_reduce(cfg, [torch.empty(0, dtype=torch.uint8, device=DEV)], [torch.empty(0, device=DEV)], 0,
+                         torch.empty(0, device=DEV))
+    n = 1000
+    g = torch.zeros(n, device=DEV)
+    err = torch.zeros(n, device=DEV)
+    codes = torch.zeros(L.loco_code_bytes(n, 4, 256), dtype=torch.uint8, device=DEV)
+    scales = torch.zeros(L.loco_num_blocks(n, 256), device=DEV)
+    with pytest.raises(L.LocoError) as ei:       # host memory
+        L.loco_compress(cfg, g.cpu(), err, 1, codes, scales)
+    assert ei.value.status == L.LOCO_ERR_INVALID_ARG
+    with pytest.raises(L.LocoError) as ei:       # buffer far shorter than n needs
+        L.loco_compress(cfg, g, err, 1, codes, scales, n=1 << 40)
+    assert ei.value.status == L.LOCO_ERR_INVALID_ARG
+    with pytest.raises(L.LocoError) as ei:       # misaligned
+        L.loco_compress(cfg, g.data_ptr() + 4, err, 1, codes, scales, n=n - 8, grad_dtype=L.LOCO_F32)
+    assert ei.value.status == L.LOCO_ERR_MISALIGNED
+    with pytest.raises(L.LocoError) as ei:       # overlapping in/out
+        L.loco_compress(cfg, g, g, 1, codes, scales)
+    assert ei.value.status == L.LOCO_ERR_INVALID_ARG
+    with pytest.raises(L.LocoError) as ei:
+        L.loco_decode_reduce(cfg, [codes] * 17, [scales] * 17, n, g)
+    assert ei.value.status == L.LOCO_ERR_UNSUPPORTED
+    # nothing was launched by the rejected calls, and the stream is still healthy
+    torch.cuda.synchronize()
+    assert not err.any()
