@@ -29,11 +29,11 @@ static loco_status fail(loco_status st, const char* fmt, ...) {
   return st;
 }
 
-int persistent_grid(const void* kernel, int threads) {
+int persistent_grid(const void* kernel, int threads, size_t smem_bytes) {
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem_bytes);
   if (sms <= 0) sms = 1;
   if (per_sm <= 0) per_sm = 1;
   return sms * per_sm;

@@ -36,41 +36,136 @@ __device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint2* p, uint2 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint32_t* p, uint32_t v) { __stcs(p, v); }
 
-// Decode the 8 codes of one 8-element chunk into floats q (exact integers).
-//  4 bit: one 32-bit word, element j in nibble j (two's complement).
-//  8 bit: two 32-bit words, element j in byte j.
-// XOR with the sign bit of each field turns two's complement into an offset
-// code (q + 8 or q + 128); OR-ing that under the exponent of 2^23 and
-// subtracting 2^23 + offset gives q exactly.
-template <int BITS>
-struct ChunkCodes;
+// ---------------------------------------------------------------------------
+// Asynchronous global -> shared copies (cp.async).  Each thread copies the
+// bytes it will itself consume and waits with cp.async.wait_group, so the
+// staging needs neither block barriers nor spin-waits; the bytes in flight
+// live in shared memory instead of registers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-template <>
-struct ChunkCodes<4> {
-  uint32_t w;
-  __device__ __forceinline__ void load(const uint8_t* base, int64_t e0) {
-    w = ld_stream(reinterpret_cast<const uint32_t*>(base + (e0 >> 1)));
-  }
-  __device__ __forceinline__ void decode(float q[8]) const {
-    const uint32_t u = w ^ 0x88888888u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      q[j] = __fsub_rn(__uint_as_float(kTwo23Bits | ((u >> (4 * j)) & 0xFu)), 8388616.0f);
-  }
-};
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs.  add.rn.f32x2 / mul.rn.f32x2 (sm_100+) each round every
+// lane exactly like the scalar add.rn / mul.rn and issue once per pair.  A
+// packed multiply whose result feeds a packed add, however, was measured to be
+// combined into a single fused multiply-add (one rounding) by the code
+// generator even with .rn and -fmad=false.  So packed ops are used only where
+// no product feeds an add: the offset subtraction of the decode (its input
+// comes from a byte permute) and the final scaling by 1/W.  Products and the
+// rank sum use the scalar __fmul_rn / __fadd_rn, which are never contracted.
+// ---------------------------------------------------------------------------
+typedef unsigned long long f32x2;
 
-template <>
-struct ChunkCodes<8> {
-  uint2 w;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f32x2 pk2u(uint32_t lo, uint32_t hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Codes of one E-element chunk of one rank (E*BITS/8 bytes: one 4- or 8-byte
+// load), decoded to packed pairs of exact floats f32(q).
+//
+// XOR with the sign bit of every field turns two's complement into the offset
+// code q + 2^(p-1); a byte permute places that byte under the exponent of 2^23
+// (bits 0x4B0000xx = 2^23 + xx exactly), and one packed subtraction of
+// 2^23 + 2^(p-1) leaves q.  4-bit fields are first split into the even and
+// odd nibbles of each byte so every element is one byte.
+// ---------------------------------------------------------------------------
+template <int BITS, int E>
+struct ChunkCodes {
+  static constexpr int kWords = E * BITS / 32;  // 32-bit words per rank
+  static_assert(kWords == 1 || kWords == 2, "one 4- or 8-byte load per rank");
+  uint32_t w[kWords];
+
+  static constexpr int kBytes = kWords * 4;
+
   __device__ __forceinline__ void load(const uint8_t* base, int64_t e0) {
-    w = ld_stream(reinterpret_cast<const uint2*>(base + e0));
+    const uint8_t* p = base + (e0 * BITS >> 3);
+    if constexpr (kWords == 1) {
+      w[0] = ld_stream(reinterpret_cast<const uint32_t*>(p));
+    } else {
+      const uint2 v = ld_stream(reinterpret_cast<const uint2*>(p));
+      w[0] = v.x;
+      w[1] = v.y;
+    }
   }
-  __device__ __forceinline__ void decode(float q[8]) const {
-    const uint32_t u0 = w.x ^ 0x80808080u, u1 = w.y ^ 0x80808080u;
+
+  // Start an asynchronous copy of this chunk's codes into shared memory.
+  __device__ __forceinline__ static void prefetch(uint8_t* dst, const uint8_t* base, int64_t e0) {
+    const uint8_t* p = base + (e0 * BITS >> 3);
+    if constexpr (kWords == 1)
+      cp_async4(dst, p);
+    else
+      cp_async8(dst, p);
+  }
+
+  __device__ __forceinline__ void load_shared(const uint8_t* src) {
+    if constexpr (kWords == 1) {
+      w[0] = *reinterpret_cast<const uint32_t*>(src);
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(src);
+      w[0] = v.x;
+      w[1] = v.y;
+    }
+  }
+
+  // q2[j] holds elements (2j, 2j+1) as floats q exactly.
+  __device__ __forceinline__ void decode(f32x2 q2[E / 2]) const {
+    constexpr uint32_t K = 0x4B000000u;
+    if constexpr (BITS == 4) {
+      const f32x2 off = pk2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      q[j] = __fsub_rn(__uint_as_float(kTwo23Bits | ((u0 >> (8 * j)) & 0xFFu)), 8388736.0f);
-      q[j + 4] = __fsub_rn(__uint_as_float(kTwo23Bits | ((u1 >> (8 * j)) & 0xFFu)), 8388736.0f);
+      for (int i = 0; i < kWords; ++i) {
+        const uint32_t u = w[i] ^ 0x88888888u;
+        const uint32_t ev = u & 0x0F0F0F0Fu;          // nibbles 0,2,4,6 -> bytes 0..3
+        const uint32_t od = (u >> 4) & 0x0F0F0F0Fu;   // nibbles 1,3,5,7 -> bytes 0..3
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          q2[4 * i + k] = add2(pk2u(__byte_perm(ev, K, 0x7440 | k), __byte_perm(od, K, 0x7440 | k)), off);
+      }
+    } else {
+      const f32x2 off = pk2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+#pragma unroll
+      for (int i = 0; i < kWords; ++i) {
+        const uint32_t u = w[i] ^ 0x80808080u;
+        q2[2 * i] = add2(pk2u(__byte_perm(u, K, 0x7440), __byte_perm(u, K, 0x7441)), off);
+        q2[2 * i + 1] = add2(pk2u(__byte_perm(u, K, 0x7442), __byte_perm(u, K, 0x7443)), off);
+      }
     }
   }
 };
@@ -78,37 +173,50 @@ struct ChunkCodes<8> {
 // Division by W: for a power of two, multiplying by the exact reciprocal gives
 // the same correctly rounded quotient; otherwise an IEEE division.
 template <int W>
-__device__ __forceinline__ float div_by_ranks(float x) {
+__device__ __forceinline__ void div_by_ranks(float a, float b, float& lo, float& hi) {
   if constexpr ((W & (W - 1)) == 0) {
-    return __fmul_rn(x, 1.0f / float(W));
+    upk2(mul2(pk2(a, b), pk2(1.0f / float(W), 1.0f / float(W))), lo, hi);
   } else {
-    return __fdiv_rn(x, float(W));
+    lo = __fdiv_rn(a, float(W));
+    hi = __fdiv_rn(b, float(W));
   }
 }
 
-// Per-element fp32 rank average of Eqn (8), in rank order 0..W-1.
-template <int BITS, int W>
-__device__ __forceinline__ void decode_mean8(const RankPtrs& rp, int64_t e0, int64_t blk, float out[8]) {
-  ChunkCodes<BITS> cw[W];
+// Per-element fp32 rank average of Eqn (8) for an E-element chunk from its
+// W ranks' codes and steps, in rank order 0..W-1:
+//   ((d_0 + d_1) + d_2) + ... , d_w = f32(q_w) * Delta_w, then / W.
+template <int BITS, int W, int E>
+__device__ __forceinline__ void mean_of_codes(const ChunkCodes<BITS, E> (&cw)[W], const float (&s)[W], float out[E]) {
+  float acc[E];
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    f32x2 q2[E / 2];
+    cw[w].decode(q2);
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j) {
+      float qa, qb;
+      upk2(q2[j], qa, qb);
+      const float da = __fmul_rn(qa, s[w]);
+      const float db = __fmul_rn(qb, s[w]);
+      acc[2 * j] = (w == 0) ? da : __fadd_rn(acc[2 * j], da);
+      acc[2 * j + 1] = (w == 0) ? db : __fadd_rn(acc[2 * j + 1], db);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < E / 2; ++j) div_by_ranks<W>(acc[2 * j], acc[2 * j + 1], out[2 * j], out[2 * j + 1]);
+}
+
+// Same, loading the codes straight from global memory (chunk at e0, block blk).
+template <int BITS, int W, int E>
+__device__ __forceinline__ void decode_mean(const RankPtrs& rp, int64_t e0, int64_t blk, float out[E]) {
+  ChunkCodes<BITS, E> cw[W];
   float s[W];
 #pragma unroll
   for (int w = 0; w < W; ++w) {
     cw[w].load(rp.codes[w], e0);
     s[w] = __ldg(rp.scales[w] + blk);
   }
-  float acc[8];
-#pragma unroll
-  for (int w = 0; w < W; ++w) {
-    float q[8];
-    cw[w].decode(q);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float d = __fmul_rn(q[j], s[w]);
-      acc[j] = (w == 0) ? d : __fadd_rn(acc[j], d);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) out[j] = div_by_ranks<W>(acc[j]);
+  mean_of_codes<BITS, W, E>(cw, s, out);
 }
 
 }  // namespace loco

@@ -65,6 +65,6 @@ cudaError_t launch_decode_reduce(const ReduceArgs& a, cudaStream_t s);
 cudaError_t launch_adam(const AdamArgs& a, cudaStream_t s);
 
 // Number of CTAs for a grid-stride kernel: resident CTAs per SM x SMs.
-int persistent_grid(const void* kernel, int threads);
+int persistent_grid(const void* kernel, int threads, size_t smem_bytes = 0);
 
 }  // namespace loco

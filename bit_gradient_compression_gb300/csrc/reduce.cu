@@ -3,32 +3,108 @@
 // §3.3 Eqn 8), optionally feeding the average straight into one Adam(W) step
 // (§4 Eqn 9) so that it never touches HBM.
 //
-// Mapping: one thread owns 8 consecutive elements: per rank one 4-byte (4-bit)
-// or 8-byte (8-bit) code load plus one scale load (shared by the B/8 threads
-// of a quant block, served by L1); all W loads are issued before any decode.
+// Mapping: one thread owns E consecutive elements: per rank one 4- or 8-byte
+// code load plus one scale load (shared by the B/E threads of a quant block,
+// served by L1); all W loads are issued before any decode.
 // The rank count W is a template parameter so the rank loop unrolls fully and
 // the loads of every rank are in flight together.
 #include "device_common.cuh"
 
 namespace loco {
 
-template <int BITS, int W>
-__global__ void __launch_bounds__(256) k_decode_reduce(const ReduceArgs a, int log2_block) {
-  const int64_t nchunks = (a.n + 7) >> 3;
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
-    const int64_t e0 = c << 3;
-    float mean[8];
-    decode_mean8<BITS, W>(a.ranks, e0, e0 >> log2_block, mean);
-    if (e0 + 8 <= a.n) {
-      float4* mp = reinterpret_cast<float4*>(a.mean + e0);
-      st_stream(mp, make_float4(mean[0], mean[1], mean[2], mean[3]));
-      st_stream(mp + 1, make_float4(mean[4], mean[5], mean[6], mean[7]));
-    } else {
+// E-element vector helpers (E a multiple of 4, 16-byte aligned when full).
+template <int E>
+__device__ __forceinline__ void load_vec(const float* p, int64_t e0, int64_t n, bool full, float x[E]) {
+  if (full) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (e0 + j < a.n) a.mean[e0 + j] = mean[j];
+    for (int i = 0; i < E / 4; ++i) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(p + e0) + i);
+      x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) x[j] = (e0 + j < n) ? p[e0 + j] : 0.0f;
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void store_vec(float* p, int64_t e0, int64_t n, bool full, const float x[E]) {
+  if (full) {
+#pragma unroll
+    for (int i = 0; i < E / 4; ++i)
+      st_stream(reinterpret_cast<float4*>(p + e0) + i, make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+      if (e0 + j < n) p[e0 + j] = x[j];
+  }
+}
+
+constexpr int kThreads = 256;
+
+// Shared-memory staging area of one CTA: S stages, each holding, per thread,
+// NF fp32 arrays of E elements (as E/4 16-byte slots, slot-major so a warp's
+// 16-byte accesses are contiguous) and W ranks' E-element code chunks.
+template <int BITS, int W, int E, int S, int NF>
+struct Staging {
+  static constexpr int CB = ChunkCodes<BITS, E>::kBytes;
+  static constexpr int F4 = E / 4;
+  static constexpr size_t kFloatBytes = size_t(S) * NF * F4 * kThreads * 16;
+  static constexpr size_t kBytes = kFloatBytes + size_t(S) * W * kThreads * CB;
+  __device__ static float4* slot(uint8_t* sm, int stage, int arr, int q, int t) {
+    return reinterpret_cast<float4*>(sm) + ((stage * NF + arr) * F4 + q) * kThreads + t;
+  }
+  __device__ static uint8_t* code(uint8_t* sm, int stage, int w, int t) {
+    return sm + kFloatBytes + ((size_t(stage) * W + w) * kThreads + t) * CB;
+  }
+};
+
+// Receiver average (Eqn 8).  Each thread walks its full E-element chunks
+// grid-stride and keeps the codes of its next S-1 chunks in flight through
+// cp.async; the one ragged chunk at the end (if any) is decoded from global
+// memory by the thread whose stride sequence reaches it.
+template <int BITS, int W, int E, int S>
+__global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, int log2_block) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  using St = Staging<BITS, W, E, S, 0>;
+  using CC = ChunkCodes<BITS, E>;
+  const int t = threadIdx.x;
+  const int64_t nfull = a.n / E;
+  const int64_t stride = int64_t(gridDim.x) * kThreads;
+  const int64_t c0 = int64_t(blockIdx.x) * kThreads + t;
+
+  auto issue = [&](int stage, int64_t c) {
+    if (c < nfull) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) CC::prefetch(St::code(sm, stage, w, t), a.ranks.codes[w], c * E);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < S - 1; ++k) issue(k, c0 + k * stride);
+  int stage = 0;
+  for (int64_t c = c0; c < nfull; c += stride) {
+    issue(stage == 0 ? S - 1 : stage - 1, c + (S - 1) * stride);
+    cp_async_wait<S - 1>();
+    const int64_t e0 = c * E;
+    CC cw[W];
+    float sc[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      cw[w].load_shared(St::code(sm, stage, w, t));
+      sc[w] = __ldg(a.ranks.scales[w] + (e0 >> log2_block));
+    }
+    float mean[E];
+    mean_of_codes<BITS, W, E>(cw, sc, mean);
+    store_vec<E>(a.mean, e0, a.n, true, mean);
+    stage = (stage + 1 == S) ? 0 : stage + 1;
+  }
+  cp_async_wait<0>();
+  if (nfull * E < a.n && c0 == nfull % stride) {
+    const int64_t e0 = nfull * E;
+    float mean[E];
+    decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, mean);
+    store_vec<E>(a.mean, e0, a.n, false, mean);
   }
 }
 
@@ -43,57 +119,78 @@ __device__ __forceinline__ void adam_elem(const AdamArgs& a, float g, float& p, 
   p = __fsub_rn(p, __fmul_rn(a.lr, __fdiv_rn(mh, den)));
 }
 
-template <int BITS, int W>
-__global__ void __launch_bounds__(256) k_adam(const AdamArgs a, int log2_block) {
-  const int64_t nchunks = (a.n + 7) >> 3;
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
-    const int64_t e0 = c << 3;
-    const bool full = e0 + 8 <= a.n;
-    float p[8], m[8], v[8];
-    if (full) {
-      const float4* pp = reinterpret_cast<const float4*>(a.param + e0);
-      const float4* mp = reinterpret_cast<const float4*>(a.m + e0);
-      const float4* vp = reinterpret_cast<const float4*>(a.v + e0);
-      const float4 p0 = __ldcs(pp), p1 = __ldcs(pp + 1);
-      const float4 m0 = __ldcs(mp), m1 = __ldcs(mp + 1);
-      const float4 v0 = __ldcs(vp), v1 = __ldcs(vp + 1);
-      p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w; p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
-      m[0] = m0.x; m[1] = m0.y; m[2] = m0.z; m[3] = m0.w; m[4] = m1.x; m[5] = m1.y; m[6] = m1.z; m[7] = m1.w;
-      v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w; v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
-    } else {
+// Receiver average fed to Adam (Eqns 8, 9).  param, m, v and the W code
+// chunks of the next S-1 chunks are staged through cp.async; the updated
+// param, m, v go straight back to global memory.
+template <int BITS, int W, int E, int S>
+__global__ void __launch_bounds__(kThreads) k_adam(const AdamArgs a, int log2_block) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  using St = Staging<BITS, W, E, S, 3>;
+  using CC = ChunkCodes<BITS, E>;
+  const int t = threadIdx.x;
+  const int64_t nfull = a.n / E;
+  const int64_t stride = int64_t(gridDim.x) * kThreads;
+  const int64_t c0 = int64_t(blockIdx.x) * kThreads + t;
+
+  auto issue = [&](int stage, int64_t c) {
+    if (c < nfull) {
+      const int64_t e0 = c * E;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool in = e0 + j < a.n;
-        p[j] = in ? a.param[e0 + j] : 0.0f;
-        m[j] = in ? a.m[e0 + j] : 0.0f;
-        v[j] = in ? a.v[e0 + j] : 0.0f;
+      for (int q = 0; q < E / 4; ++q) {
+        cp_async16(St::slot(sm, stage, 0, q, t), a.param + e0 + 4 * q);
+        cp_async16(St::slot(sm, stage, 1, q, t), a.m + e0 + 4 * q);
+        cp_async16(St::slot(sm, stage, 2, q, t), a.v + e0 + 4 * q);
       }
-    }
-    float g[8];
-    decode_mean8<BITS, W>(a.ranks, e0, e0 >> log2_block, g);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
-    if (full) {
-      float4* pp = reinterpret_cast<float4*>(a.param + e0);
-      float4* mp = reinterpret_cast<float4*>(a.m + e0);
-      float4* vp = reinterpret_cast<float4*>(a.v + e0);
-      st_stream(pp, make_float4(p[0], p[1], p[2], p[3]));
-      st_stream(pp + 1, make_float4(p[4], p[5], p[6], p[7]));
-      st_stream(mp, make_float4(m[0], m[1], m[2], m[3]));
-      st_stream(mp + 1, make_float4(m[4], m[5], m[6], m[7]));
-      st_stream(vp, make_float4(v[0], v[1], v[2], v[3]));
-      st_stream(vp + 1, make_float4(v[4], v[5], v[6], v[7]));
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (e0 + j < a.n) {
-          a.param[e0 + j] = p[j];
-          a.m[e0 + j] = m[j];
-          a.v[e0 + j] = v[j];
-        }
-      }
+      for (int w = 0; w < W; ++w) CC::prefetch(St::code(sm, stage, w, t), a.ranks.codes[w], e0);
     }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < S - 1; ++k) issue(k, c0 + k * stride);
+  int stage = 0;
+  for (int64_t c = c0; c < nfull; c += stride) {
+    issue(stage == 0 ? S - 1 : stage - 1, c + (S - 1) * stride);
+    cp_async_wait<S - 1>();
+    const int64_t e0 = c * E;
+    float p[E], m[E], v[E], g[E];
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      const float4 pv = *St::slot(sm, stage, 0, q, t);
+      const float4 mv = *St::slot(sm, stage, 1, q, t);
+      const float4 vv = *St::slot(sm, stage, 2, q, t);
+      p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
+      m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
+      v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
+    }
+    CC cw[W];
+    float sc[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      cw[w].load_shared(St::code(sm, stage, w, t));
+      sc[w] = __ldg(a.ranks.scales[w] + (e0 >> log2_block));
+    }
+    mean_of_codes<BITS, W, E>(cw, sc, g);
+#pragma unroll
+    for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+    store_vec<E>(a.param, e0, a.n, true, p);
+    store_vec<E>(a.m, e0, a.n, true, m);
+    store_vec<E>(a.v, e0, a.n, true, v);
+    stage = (stage + 1 == S) ? 0 : stage + 1;
+  }
+  cp_async_wait<0>();
+  if (nfull * E < a.n && c0 == nfull % stride) {
+    const int64_t e0 = nfull * E;
+    float p[E], m[E], v[E], g[E];
+    load_vec<E>(a.param, e0, a.n, false, p);
+    load_vec<E>(a.m, e0, a.n, false, m);
+    load_vec<E>(a.v, e0, a.n, false, v);
+    decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
+#pragma unroll
+    for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+    store_vec<E>(a.param, e0, a.n, false, p);
+    store_vec<E>(a.m, e0, a.n, false, m);
+    store_vec<E>(a.v, e0, a.n, false, v);
   }
 }
 
@@ -103,21 +200,41 @@ static int ilog2(int x) {
   return r;
 }
 
+#ifndef LOCO_REDUCE_ELEMS
+#define LOCO_REDUCE_ELEMS(bits) (64 / (bits))  // elements per thread chunk: 8 code bytes per rank
+#endif
+#ifndef LOCO_REDUCE_STAGES
+#define LOCO_REDUCE_STAGES 4
+#endif
+#ifndef LOCO_ADAM_ELEMS
+#define LOCO_ADAM_ELEMS(bits) 8
+#endif
+#ifndef LOCO_ADAM_STAGES
+#define LOCO_ADAM_STAGES 3
+#endif
+
 template <typename Args, int BITS, int W, bool ADAM>
 static cudaError_t launch_w(const Args& a, cudaStream_t s) {
+  constexpr int E = ADAM ? LOCO_ADAM_ELEMS(BITS) : LOCO_REDUCE_ELEMS(BITS);
+  constexpr int S = ADAM ? LOCO_ADAM_STAGES : LOCO_REDUCE_STAGES;
+  constexpr size_t smem = ADAM ? Staging<BITS, W, E, S, 3>::kBytes : Staging<BITS, W, E, S, 0>::kBytes;
+  static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
   const void* fn;
   if constexpr (ADAM)
-    fn = reinterpret_cast<const void*>(&k_adam<BITS, W>);
+    fn = reinterpret_cast<const void*>(&k_adam<BITS, W, E, S>);
   else
-    fn = reinterpret_cast<const void*>(&k_decode_reduce<BITS, W>);
-  static const int cap = persistent_grid(fn, 256);
-  const int64_t nchunks = (a.n + 7) >> 3;
-  const int64_t ctas_needed = (nchunks + 255) / 256;
+    fn = reinterpret_cast<const void*>(&k_decode_reduce<BITS, W, E, S>);
+  static const int cap = [&] {
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    return persistent_grid(fn, kThreads, smem);
+  }();
+  const int64_t nchunks = (a.n + E - 1) / E;
+  const int64_t ctas_needed = (nchunks + kThreads - 1) / kThreads;
   const int grid = int(ctas_needed < cap ? ctas_needed : cap);
   if constexpr (ADAM)
-    k_adam<BITS, W><<<grid, 256, 0, s>>>(a, ilog2(a.block));
+    k_adam<BITS, W, E, S><<<grid, kThreads, smem, s>>>(a, ilog2(a.block));
   else
-    k_decode_reduce<BITS, W><<<grid, 256, 0, s>>>(a, ilog2(a.block));
+    k_decode_reduce<BITS, W, E, S><<<grid, kThreads, smem, s>>>(a, ilog2(a.block));
   return cudaGetLastError();
 }
 
