@@ -50,14 +50,15 @@ def _headers():
     return hs
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = LIB, build_dir: str = BUILD) -> str:
+    """Compile the sources into build_dir and link them into out (default: in-tree libloco.so)."""
+    os.makedirs(build_dir, exist_ok=True)
     headers = _headers()
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s, *headers]):
             cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o]
@@ -71,11 +72,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                     sys.stderr.write(" ".join(c) + "\n" + r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed on {c[-3]}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(out, objs):
+        tmp = out + f".tmp{os.getpid()}"
         subprocess.check_call([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -297,14 +297,19 @@ loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes, 
   a.param = param;
   a.m = m;
   a.v = v;
-  a.lr = hp->lr;
   a.beta1 = hp->beta1;
   a.beta2 = hp->beta2;
   a.one_minus_beta1 = 1.0f - hp->beta1;
   a.one_minus_beta2 = 1.0f - hp->beta2;
   a.lr_wd = hp->lr * hp->weight_decay;
-  a.bc1 = hp->bias_correction ? float(1.0 - pow(double(hp->beta1), double(t))) : 1.0f;
-  a.bc2 = hp->bias_correction ? float(1.0 - pow(double(hp->beta2), double(t))) : 1.0f;
+  a.c1 = hp->lr;
+  a.c2 = 1.0f;
+  if (hp->bias_correction) {
+    const double bc1 = 1.0 - pow(double(hp->beta1), double(t));
+    const double bc2 = 1.0 - pow(double(hp->beta2), double(t));
+    a.c1 = float(double(hp->lr) / bc1);
+    a.c2 = hp->eps_inside_sqrt ? float(1.0 / bc2) : float(1.0 / sqrt(bc2));
+  }
   a.eps = hp->eps;
   a.eps_inside_sqrt = hp->eps_inside_sqrt != 0;
   return launch_result(launch_adam(a, reinterpret_cast<cudaStream_t>(stream)), "loco_adam_step");

@@ -51,11 +51,11 @@ struct AdamArgs {
   float* param;
   float* m;
   float* v;
-  float lr;
   float beta1, beta2;
   float one_minus_beta1, one_minus_beta2;
   float lr_wd;
-  float bc1, bc2;
+  float c1;  // lr / (1 - beta1^t)
+  float c2;  // 1 / sqrt(1 - beta2^t), or 1 / (1 - beta2^t) with eps inside the root
   float eps;
   int eps_inside_sqrt;
 };

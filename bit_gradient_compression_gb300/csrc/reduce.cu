@@ -3,11 +3,10 @@
 // §3.3 Eqn 8), optionally feeding the average straight into one Adam(W) step
 // (§4 Eqn 9) so that it never touches HBM.
 //
-// Mapping: one thread owns E consecutive elements: per rank one 4- or 8-byte
-// code load plus one scale load (shared by the B/E threads of a quant block,
-// served by L1); all W loads are issued before any decode.
-// The rank count W is a template parameter so the rank loop unrolls fully and
-// the loads of every rank are in flight together.
+// Mapping: a CTA of 256 threads consumes tiles of 256*E elements staged in
+// shared memory by a multistage cp.async pipeline (coalesced 16-byte pieces of
+// every input of the tile); thread t owns elements [t*E, t*E + E) of a tile.
+// The rank count W is a template parameter so the rank loop unrolls fully.
 #include "device_common.cuh"
 
 namespace loco {
@@ -42,70 +41,131 @@ __device__ __forceinline__ void store_vec(float* p, int64_t e0, int64_t n, bool 
 
 constexpr int kThreads = 256;
 
-// Shared-memory staging area of one CTA: S stages, each holding, per thread,
-// NF fp32 arrays of E elements (as E/4 16-byte slots, slot-major so a warp's
-// 16-byte accesses are contiguous) and W ranks' E-element code chunks.
-template <int BITS, int W, int E, int S, int NF>
-struct Staging {
-  static constexpr int CB = ChunkCodes<BITS, E>::kBytes;
-  static constexpr int F4 = E / 4;
-  static constexpr size_t kFloatBytes = size_t(S) * NF * F4 * kThreads * 16;
-  static constexpr size_t kBytes = kFloatBytes + size_t(S) * W * kThreads * CB;
-  __device__ static float4* slot(uint8_t* sm, int stage, int arr, int q, int t) {
-    return reinterpret_cast<float4*>(sm) + ((stage * NF + arr) * F4 + q) * kThreads + t;
-  }
-  __device__ static uint8_t* code(uint8_t* sm, int stage, int w, int t) {
-    return sm + kFloatBytes + ((size_t(stage) * W + w) * kThreads + t) * CB;
+// Shared-memory image of one tile of T = 256*E elements: NF fp32 arrays
+// (T floats each), W ranks' packed codes (T*BITS/8 bytes each) and W ranks'
+// steps (T/block floats each, room for the smallest block of 64).
+template <int BITS, int W, int E, int NF>
+struct Tile {
+  static constexpr int T = kThreads * E;
+  static constexpr int kCodeBytes = T * BITS / 8;
+  static constexpr int kScaleMax = T / 64;
+  static constexpr size_t kFloatBytes = size_t(NF) * T * 4;
+  static constexpr size_t kBytes = kFloatBytes + size_t(W) * kCodeBytes + size_t(W) * kScaleMax * 4;
+  uint8_t* base;
+  __device__ float* f(int arr) const { return reinterpret_cast<float*>(base) + arr * T; }
+  __device__ uint8_t* codes(int w) const { return base + kFloatBytes + w * kCodeBytes; }
+  __device__ float* scales(int w) const {
+    return reinterpret_cast<float*>(base + kFloatBytes + size_t(W) * kCodeBytes) + w * kScaleMax;
   }
 };
 
-// Receiver average (Eqn 8).  Each thread walks its full E-element chunks
-// grid-stride and keeps the codes of its next S-1 chunks in flight through
-// cp.async; the one ragged chunk at the end (if any) is decoded from global
-// memory by the thread whose stride sequence reaches it.
-template <int BITS, int W, int E, int S>
-__global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, int log2_block) {
-  extern __shared__ __align__(16) uint8_t sm[];
-  using St = Staging<BITS, W, E, S, 0>;
-  using CC = ChunkCodes<BITS, E>;
-  const int t = threadIdx.x;
-  const int64_t nfull = a.n / E;
-  const int64_t stride = int64_t(gridDim.x) * kThreads;
-  const int64_t c0 = int64_t(blockIdx.x) * kThreads + t;
+// Largest stage count <= want whose tiles fit one CTA's shared memory.
+template <int BITS, int W, int E, int NF>
+constexpr int fit_stages(int want) {
+  int s = want;
+  while (s > 1 && size_t(s) * Tile<BITS, W, E, NF>::kBytes > size_t(227) * 1024) --s;
+  return s;
+}
 
-  auto issue = [&](int stage, int64_t c) {
-    if (c < nfull) {
+// Starts the cp.async copies of tile `tile` into `dst`: every piece is 16
+// bytes and consecutive threads take consecutive pieces, so each warp moves
+// 512 contiguous bytes per instruction.  nsc = T/block steps per rank.
+template <int BITS, int W, int E, int NF>
+__device__ __forceinline__ void issue_tile(const Tile<BITS, W, E, NF>& dst, const float* const* farr,
+                                           const RankPtrs& rp, int64_t tile, int nsc, int t) {
+  using TL = Tile<BITS, W, E, NF>;
+  const int64_t e0 = tile * TL::T;
+  static_assert((TL::T / 4) % kThreads == 0, "whole 16-byte pieces per thread");
 #pragma unroll
-      for (int w = 0; w < W; ++w) CC::prefetch(St::code(sm, stage, w, t), a.ranks.codes[w], c * E);
-    }
+  for (int arr = 0; arr < NF; ++arr) {
+#pragma unroll
+    for (int q = t; q < TL::T / 4; q += kThreads) cp_async16(dst.f(arr) + 4 * q, farr[arr] + e0 + 4 * q);
+  }
+  constexpr int kCodePieces = TL::kCodeBytes / 16;
+#pragma unroll
+  for (int p = t; p < W * kCodePieces; p += kThreads) {
+    const int w = p / kCodePieces, q = p % kCodePieces;
+    cp_async16(dst.codes(w) + 16 * q, rp.codes[w] + tile * TL::kCodeBytes + 16 * q);
+  }
+  const int sc_pieces = nsc / 4;
+  for (int p = t; p < W * sc_pieces; p += kThreads) {
+    const int w = p / sc_pieces, q = p - w * sc_pieces;
+    cp_async16(dst.scales(w) + 4 * q, rp.scales[w] + tile * nsc + 4 * q);
+  }
+}
+
+// Rank average of this thread's E elements of a staged tile.
+template <int BITS, int W, int E, int NF>
+__device__ __forceinline__ void tile_mean(const Tile<BITS, W, E, NF>& tl, int t, int log2_block, float out[E]) {
+  ChunkCodes<BITS, E> cw[W];
+  float sc[W];
+  const int blk = (t * E) >> log2_block;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    cw[w].load_shared(tl.codes(w) + (t * E * BITS >> 3));
+    sc[w] = tl.scales(w)[blk];
+  }
+  mean_of_codes<BITS, W, E>(cw, sc, out);
+}
+
+// Multistage tile pipeline shared by the receiver kernels.  The CTA walks
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ...; S-1 tiles are in flight
+// while one is consumed.  cp.async.wait_group plus __syncthreads make a tile
+// visible to every thread, and a second __syncthreads keeps a stage from being
+// refilled before all threads are done with it: no spin-waits anywhere.
+// Elements past the last full tile are handled by `tail` in one CTA.
+template <int BITS, int W, int E, int NF, int S, typename Body, typename TailFn>
+__device__ __forceinline__ void tile_pipeline(const float* const* farr, const RankPtrs& rp, int64_t n, int log2_block,
+                                              Body body, TailFn tail) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  using TL = Tile<BITS, W, E, NF>;
+  const int t = threadIdx.x;
+  const int64_t ntiles = n / TL::T;
+  const int nsc = TL::T >> log2_block;
+  auto stage = [&](int s) { return TL{sm + size_t(s) * TL::kBytes}; };
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    const int64_t tile = blockIdx.x + int64_t(s) * gridDim.x;
+    if (tile < ntiles) issue_tile<BITS, W, E, NF>(stage(s), farr, rp, tile, nsc, t);
     cp_async_commit();
-  };
-#pragma unroll
-  for (int k = 0; k < S - 1; ++k) issue(k, c0 + k * stride);
-  int stage = 0;
-  for (int64_t c = c0; c < nfull; c += stride) {
-    issue(stage == 0 ? S - 1 : stage - 1, c + (S - 1) * stride);
+  }
+  int cur = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t ahead = tile + int64_t(S - 1) * gridDim.x;
+    const int nxt = (cur == 0) ? S - 1 : cur - 1;
+    if (ahead < ntiles) issue_tile<BITS, W, E, NF>(stage(nxt), farr, rp, ahead, nsc, t);
+    cp_async_commit();
     cp_async_wait<S - 1>();
-    const int64_t e0 = c * E;
-    CC cw[W];
-    float sc[W];
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      cw[w].load_shared(St::code(sm, stage, w, t));
-      sc[w] = __ldg(a.ranks.scales[w] + (e0 >> log2_block));
-    }
-    float mean[E];
-    mean_of_codes<BITS, W, E>(cw, sc, mean);
-    store_vec<E>(a.mean, e0, a.n, true, mean);
-    stage = (stage + 1 == S) ? 0 : stage + 1;
+    __syncthreads();
+    body(stage(cur), tile * TL::T + int64_t(t) * E);
+    __syncthreads();
+    cur = (cur + 1 == S) ? 0 : cur + 1;
   }
   cp_async_wait<0>();
-  if (nfull * E < a.n && c0 == nfull % stride) {
-    const int64_t e0 = nfull * E;
-    float mean[E];
-    decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, mean);
-    store_vec<E>(a.mean, e0, a.n, false, mean);
+  if (ntiles * TL::T < n && blockIdx.x == ntiles % gridDim.x) {
+    const int64_t e0 = ntiles * TL::T + int64_t(t) * E;
+    if (e0 < n) tail(e0);
   }
+}
+
+// Receiver average (Eqn 8): codes and steps staged per tile, the mean stored
+// straight from registers.
+template <int BITS, int W, int E, int S>
+__global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, int log2_block) {
+  using TL = Tile<BITS, W, E, 0>;
+  const float* none[1] = {nullptr};
+  tile_pipeline<BITS, W, E, 0, S>(
+      none, a.ranks, a.n, log2_block,
+      [&](const TL& tl, int64_t e0) {
+        float mean[E];
+        tile_mean<BITS, W, E, 0>(tl, threadIdx.x, log2_block, mean);
+        store_vec<E>(a.mean, e0, a.n, true, mean);
+      },
+      [&](int64_t e0) {
+        float mean[E];
+        decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, mean);
+        store_vec<E>(a.mean, e0, a.n, e0 + E <= a.n, mean);
+      });
 }
 
 // One Adam(W) update of one element, in the order the header states.
@@ -113,85 +173,51 @@ __device__ __forceinline__ void adam_elem(const AdamArgs& a, float g, float& p, 
   p = __fsub_rn(p, __fmul_rn(a.lr_wd, p));
   m = __fadd_rn(__fmul_rn(a.beta1, m), __fmul_rn(a.one_minus_beta1, g));
   v = __fadd_rn(__fmul_rn(a.beta2, v), __fmul_rn(a.one_minus_beta2, __fmul_rn(g, g)));
-  const float mh = __fdiv_rn(m, a.bc1);
-  const float vh = __fdiv_rn(v, a.bc2);
-  const float den = a.eps_inside_sqrt ? __fsqrt_rn(__fadd_rn(vh, a.eps)) : __fadd_rn(__fsqrt_rn(vh), a.eps);
-  p = __fsub_rn(p, __fmul_rn(a.lr, __fdiv_rn(mh, den)));
+  const float den = a.eps_inside_sqrt ? __fsqrt_rn(__fadd_rn(__fmul_rn(v, a.c2), a.eps))
+                                      : __fadd_rn(__fmul_rn(__fsqrt_rn(v), a.c2), a.eps);
+  p = __fsub_rn(p, __fmul_rn(a.c1, __fdiv_rn(m, den)));
 }
 
-// Receiver average fed to Adam (Eqns 8, 9).  param, m, v and the W code
-// chunks of the next S-1 chunks are staged through cp.async; the updated
-// param, m, v go straight back to global memory.
+// Receiver average fed to Adam (Eqns 8, 9): param, m, v, codes and steps
+// staged per tile; the updated param, m, v stored straight from registers.
 template <int BITS, int W, int E, int S>
 __global__ void __launch_bounds__(kThreads) k_adam(const AdamArgs a, int log2_block) {
-  extern __shared__ __align__(16) uint8_t sm[];
-  using St = Staging<BITS, W, E, S, 3>;
-  using CC = ChunkCodes<BITS, E>;
-  const int t = threadIdx.x;
-  const int64_t nfull = a.n / E;
-  const int64_t stride = int64_t(gridDim.x) * kThreads;
-  const int64_t c0 = int64_t(blockIdx.x) * kThreads + t;
-
-  auto issue = [&](int stage, int64_t c) {
-    if (c < nfull) {
-      const int64_t e0 = c * E;
+  using TL = Tile<BITS, W, E, 3>;
+  const float* farr[3] = {a.param, a.m, a.v};
+  tile_pipeline<BITS, W, E, 3, S>(
+      farr, a.ranks, a.n, log2_block,
+      [&](const TL& tl, int64_t e0) {
+        const int t = threadIdx.x;
+        float p[E], m[E], v[E], g[E];
 #pragma unroll
-      for (int q = 0; q < E / 4; ++q) {
-        cp_async16(St::slot(sm, stage, 0, q, t), a.param + e0 + 4 * q);
-        cp_async16(St::slot(sm, stage, 1, q, t), a.m + e0 + 4 * q);
-        cp_async16(St::slot(sm, stage, 2, q, t), a.v + e0 + 4 * q);
-      }
+        for (int q = 0; q < E / 4; ++q) {
+          const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
+          const float4 mv = reinterpret_cast<const float4*>(tl.f(1) + t * E)[q];
+          const float4 vv = reinterpret_cast<const float4*>(tl.f(2) + t * E)[q];
+          p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
+          m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
+          v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
+        }
+        tile_mean<BITS, W, E, 3>(tl, t, log2_block, g);
 #pragma unroll
-      for (int w = 0; w < W; ++w) CC::prefetch(St::code(sm, stage, w, t), a.ranks.codes[w], e0);
-    }
-    cp_async_commit();
-  };
+        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+        store_vec<E>(a.param, e0, a.n, true, p);
+        store_vec<E>(a.m, e0, a.n, true, m);
+        store_vec<E>(a.v, e0, a.n, true, v);
+      },
+      [&](int64_t e0) {
+        const bool full = e0 + E <= a.n;
+        float p[E], m[E], v[E], g[E];
+        load_vec<E>(a.param, e0, a.n, full, p);
+        load_vec<E>(a.m, e0, a.n, full, m);
+        load_vec<E>(a.v, e0, a.n, full, v);
+        decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
 #pragma unroll
-  for (int k = 0; k < S - 1; ++k) issue(k, c0 + k * stride);
-  int stage = 0;
-  for (int64_t c = c0; c < nfull; c += stride) {
-    issue(stage == 0 ? S - 1 : stage - 1, c + (S - 1) * stride);
-    cp_async_wait<S - 1>();
-    const int64_t e0 = c * E;
-    float p[E], m[E], v[E], g[E];
-#pragma unroll
-    for (int q = 0; q < E / 4; ++q) {
-      const float4 pv = *St::slot(sm, stage, 0, q, t);
-      const float4 mv = *St::slot(sm, stage, 1, q, t);
-      const float4 vv = *St::slot(sm, stage, 2, q, t);
-      p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
-      m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
-      v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
-    }
-    CC cw[W];
-    float sc[W];
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      cw[w].load_shared(St::code(sm, stage, w, t));
-      sc[w] = __ldg(a.ranks.scales[w] + (e0 >> log2_block));
-    }
-    mean_of_codes<BITS, W, E>(cw, sc, g);
-#pragma unroll
-    for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
-    store_vec<E>(a.param, e0, a.n, true, p);
-    store_vec<E>(a.m, e0, a.n, true, m);
-    store_vec<E>(a.v, e0, a.n, true, v);
-    stage = (stage + 1 == S) ? 0 : stage + 1;
-  }
-  cp_async_wait<0>();
-  if (nfull * E < a.n && c0 == nfull % stride) {
-    const int64_t e0 = nfull * E;
-    float p[E], m[E], v[E], g[E];
-    load_vec<E>(a.param, e0, a.n, false, p);
-    load_vec<E>(a.m, e0, a.n, false, m);
-    load_vec<E>(a.v, e0, a.n, false, v);
-    decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
-#pragma unroll
-    for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
-    store_vec<E>(a.param, e0, a.n, false, p);
-    store_vec<E>(a.m, e0, a.n, false, m);
-    store_vec<E>(a.v, e0, a.n, false, v);
-  }
+        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+        store_vec<E>(a.param, e0, a.n, full, p);
+        store_vec<E>(a.m, e0, a.n, full, m);
+        store_vec<E>(a.v, e0, a.n, full, v);
+      });
 }
 
 static int ilog2(int x) {
@@ -210,14 +236,14 @@ static int ilog2(int x) {
 #define LOCO_ADAM_ELEMS(bits) 8
 #endif
 #ifndef LOCO_ADAM_STAGES
-#define LOCO_ADAM_STAGES 3
+#define LOCO_ADAM_STAGES 2
 #endif
 
 template <typename Args, int BITS, int W, bool ADAM>
 static cudaError_t launch_w(const Args& a, cudaStream_t s) {
   constexpr int E = ADAM ? LOCO_ADAM_ELEMS(BITS) : LOCO_REDUCE_ELEMS(BITS);
-  constexpr int S = ADAM ? LOCO_ADAM_STAGES : LOCO_REDUCE_STAGES;
-  constexpr size_t smem = ADAM ? Staging<BITS, W, E, S, 3>::kBytes : Staging<BITS, W, E, S, 0>::kBytes;
+  constexpr int S = ADAM ? fit_stages<BITS, W, E, 3>(LOCO_ADAM_STAGES) : fit_stages<BITS, W, E, 0>(LOCO_REDUCE_STAGES);
+  constexpr size_t smem = S * (ADAM ? Tile<BITS, W, E, 3>::kBytes : Tile<BITS, W, E, 0>::kBytes);
   static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
   const void* fn;
   if constexpr (ADAM)

@@ -79,7 +79,7 @@ typedef struct {
   float   beta2;           /* weight of the previous v: v = beta2*v + (1-beta2)*g*g             */
   float   eps;             /* delta                                                             */
   float   weight_decay;    /* decoupled (AdamW) decay; 0 = plain Adam                           */
-  int32_t bias_correction; /* 1: divide m, v by 1-beta^t; 0: no correction                      */
+  int32_t bias_correction; /* 1: bias-corrected step (c1, c2 of loco_adam_step); 0: c1=lr, c2=1  */
   int32_t eps_inside_sqrt; /* 1: 1/sqrt(v+eps) as printed in §4; 0: 1/(sqrt(v)+eps) as in Adam  */
 } loco_adam_hparams;
 
@@ -141,17 +141,20 @@ loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* cod
  * loco_adam_step — loco_decode_reduce fused with one Adam(W) update of the
  * rank's parameters (§4, Eqn 9: the optimizer consumes the averaged low-bit
  * gradient g~ of Eqn 8).  g~_i is formed exactly as in loco_decode_reduce and
- * is never written to memory.  Per element, in this order:
+ * is never written to memory.  Per element, in this order (Kingma & Ba's Adam
+ * with decoupled weight decay, bias corrections folded into the step size and
+ * the denominator as in their Algorithm 1):
  *   p   = p - (lr*wd)*p
  *   m   = beta1*m + (1-beta1)*g~
  *   v   = beta2*v + (1-beta2)*(g~*g~)
- *   mh  = m / bc1 ; vh = v / bc2     (bc = f32(1 - beta^t) in double, or 1)
- *   den = sqrt(vh) + eps   (eps_inside_sqrt: sqrt(vh + eps))
- *   p   = p - lr*(mh/den)
- * lr*wd, 1-beta1 and 1-beta2 are formed once in fp32.  The paper's own
- * convention (beta on the new term, no bias correction, 1/sqrt(v+delta)) is
- * beta1 = 1-0.1, beta2 = 1-beta2_paper, bias_correction = 0,
- * eps_inside_sqrt = 1.
+ *   den = sqrt(v)*c2 + eps        c2 = 1/sqrt(1 - beta2^t)
+ *        (eps_inside_sqrt: den = sqrt(v*c2 + eps), c2 = 1/(1 - beta2^t))
+ *   p   = p - c1*(m/den)          c1 = lr/(1 - beta1^t)
+ * lr*wd, 1-beta1 and 1-beta2 are formed once in fp32; c1 and c2 once in
+ * double from the fp32 hyper-parameters, rounded to fp32 (c1 = lr, c2 = 1
+ * without bias correction).  The paper's own convention (beta on the new
+ * term, no bias correction, 1/sqrt(v+delta)) is beta1 = 1-0.1,
+ * beta2 = 1-beta2_paper, bias_correction = 0, eps_inside_sqrt = 1.
  * param, m, v [n] device fp32, in/out.  t = 1-based optimizer step.
  */
 loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes,

@@ -190,12 +190,17 @@ void oracle_decode_reduce(int bits, int block, const uint8_t* const* codes,
  * Receiver step fused with the optimizer, §4 Eqn (9): the averaged low-bit
  * gradient g~ of Eqn (8) drives one Adam(W) update of param, m, v for the
  * elements [i0, i1).  g~ is formed exactly as in oracle_decode_reduce.
- * The update (Kingma & Ba's Adam with decoupled weight decay):
- *   p = p - (lr*wd)*p ; m = beta1*m + (1-beta1)*g ; v = beta2*v + (1-beta2)*g*g
- *   mh = m/bc1 ; vh = v/bc2 ; den = sqrt(vh)+eps (or sqrt(vh+eps)) ;
- *   p = p - lr*(mh/den)
- * bc1, bc2 are 1 - beta^t computed in double and rounded to fp32, or 1 when
- * bias correction is off.
+ * The update is Kingma & Ba's Adam with decoupled weight decay, with the bias
+ * corrections folded into the step size and the denominator as in their
+ * Algorithm 1 (alpha_t = alpha / (1 - beta1^t), sqrt(v_t) / sqrt(1 - beta2^t)):
+ *   p   = p - (lr*wd)*p
+ *   m   = beta1*m + (1-beta1)*g
+ *   v   = beta2*v + (1-beta2)*(g*g)
+ *   den = sqrt(v)*c2 + eps            with c2 = 1/sqrt(1 - beta2^t)
+ *       (eps inside the root:  den = sqrt(v*c2 + eps) with c2 = 1/(1 - beta2^t))
+ *   p   = p - c1*(m/den)              with c1 = lr/(1 - beta1^t)
+ * c1 and c2 are computed in double from the fp32 hyper-parameters and rounded
+ * to fp32 once; without bias correction c1 = lr and c2 = 1.
  */
 void oracle_adam_step(int bits, int block, const uint8_t* const* codes,
                       const float* const* scales, int W, int64_t i0, int64_t i1,
@@ -206,10 +211,12 @@ void oracle_adam_step(int bits, int block, const uint8_t* const* codes,
   const float lr_wd = lr * wd;
   const float omb1 = 1.0f - beta1;
   const float omb2 = 1.0f - beta2;
-  float bc1 = 1.0f, bc2 = 1.0f;
+  float c1 = lr, c2 = 1.0f;
   if (bias_correction) {
-    bc1 = (float)(1.0 - pow((double)beta1, (double)t));
-    bc2 = (float)(1.0 - pow((double)beta2, (double)t));
+    double bc1 = 1.0 - pow((double)beta1, (double)t);
+    double bc2 = 1.0 - pow((double)beta2, (double)t);
+    c1 = (float)((double)lr / bc1);
+    c2 = eps_inside_sqrt ? (float)(1.0 / bc2) : (float)(1.0 / sqrt(bc2));
   }
   for (int64_t i = i0; i < i1; ++i) {
     const int64_t b = i / block;
@@ -232,18 +239,18 @@ void oracle_adam_step(int bits, int block, const uint8_t* const* codes,
     float vi = beta2 * v[i];
     float vg = omb2 * gg;
     vi = vi + vg;
-    float mh = mi / bc1;
-    float vh = vi / bc2;
     float den;
     if (eps_inside_sqrt) {
-      float s = vh + eps;
+      float vs = vi * c2;
+      float s = vs + eps;
       den = sqrtf(s);
     } else {
-      float s = sqrtf(vh);
-      den = s + eps;
+      float r = sqrtf(vi);
+      float rs = r * c2;
+      den = rs + eps;
     }
-    float ratio = mh / den;
-    float step = lr * ratio;
+    float ratio = mi / den;
+    float step = c1 * ratio;
     p = p - step;
     param[i] = p;
     m[i] = mi;
