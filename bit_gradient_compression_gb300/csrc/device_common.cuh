@@ -61,6 +61,41 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ---------------------------------------------------------------------------
+// Multistage tile pipeline.  The CTA walks tiles blockIdx.x, blockIdx.x +
+// gridDim.x, ...; S-1 tiles are in flight (cp.async into their own stage of
+// shared memory) while one is consumed.  cp.async.wait_group plus
+// __syncthreads make a tile visible to every thread, and the second
+// __syncthreads keeps a stage from being refilled before every thread is done
+// with it.  Both barriers are reached by all threads of the CTA (the loop
+// bounds are uniform), and there is no spin-wait anywhere.
+//   issue(stage_base, tile): start the copies of one tile (each thread its share)
+//   body(stage_base, tile):  consume one staged tile
+// ---------------------------------------------------------------------------
+template <int S, typename Issue, typename Body>
+__device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, int64_t ntiles, Issue issue,
+                                               Body body) {
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    const int64_t tile = blockIdx.x + int64_t(s) * gridDim.x;
+    if (tile < ntiles) issue(sm + s * stage_bytes, tile);
+    cp_async_commit();
+  }
+  int cur = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t ahead = tile + int64_t(S - 1) * gridDim.x;
+    const int nxt = (cur == 0) ? S - 1 : cur - 1;
+    if (ahead < ntiles) issue(sm + nxt * stage_bytes, ahead);
+    cp_async_commit();
+    cp_async_wait<S - 1>();
+    __syncthreads();
+    body(sm + cur * stage_bytes, tile);
+    __syncthreads();
+    cur = (cur + 1 == S) ? 0 : cur + 1;
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
 // Packed fp32 pairs.  add.rn.f32x2 / mul.rn.f32x2 (sm_100+) each round every
 // lane exactly like the scalar add.rn / mul.rn and issue once per pair.  A
 // packed multiply whose result feeds a packed add, however, was measured to be

@@ -108,12 +108,8 @@ __device__ __forceinline__ void tile_mean(const Tile<BITS, W, E, NF>& tl, int t,
   mean_of_codes<BITS, W, E>(cw, sc, out);
 }
 
-// Multistage tile pipeline shared by the receiver kernels.  The CTA walks
-// tiles blockIdx.x, blockIdx.x + gridDim.x, ...; S-1 tiles are in flight
-// while one is consumed.  cp.async.wait_group plus __syncthreads make a tile
-// visible to every thread, and a second __syncthreads keeps a stage from being
-// refilled before all threads are done with it: no spin-waits anywhere.
-// Elements past the last full tile are handled by `tail` in one CTA.
+// Receiver tiles through the multistage pipeline; elements past the last full
+// tile are handled by `tail` in one CTA.
 template <int BITS, int W, int E, int NF, int S, typename Body, typename TailFn>
 __device__ __forceinline__ void tile_pipeline(const float* const* farr, const RankPtrs& rp, int64_t n, int log2_block,
                                               Body body, TailFn tail) {
@@ -122,26 +118,10 @@ __device__ __forceinline__ void tile_pipeline(const float* const* farr, const Ra
   const int t = threadIdx.x;
   const int64_t ntiles = n / TL::T;
   const int nsc = TL::T >> log2_block;
-  auto stage = [&](int s) { return TL{sm + size_t(s) * TL::kBytes}; };
-#pragma unroll
-  for (int s = 0; s < S - 1; ++s) {
-    const int64_t tile = blockIdx.x + int64_t(s) * gridDim.x;
-    if (tile < ntiles) issue_tile<BITS, W, E, NF>(stage(s), farr, rp, tile, nsc, t);
-    cp_async_commit();
-  }
-  int cur = 0;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int64_t ahead = tile + int64_t(S - 1) * gridDim.x;
-    const int nxt = (cur == 0) ? S - 1 : cur - 1;
-    if (ahead < ntiles) issue_tile<BITS, W, E, NF>(stage(nxt), farr, rp, ahead, nsc, t);
-    cp_async_commit();
-    cp_async_wait<S - 1>();
-    __syncthreads();
-    body(stage(cur), tile * TL::T + int64_t(t) * E);
-    __syncthreads();
-    cur = (cur + 1 == S) ? 0 : cur + 1;
-  }
-  cp_async_wait<0>();
+  pipeline_tiles<S>(
+      sm, TL::kBytes, ntiles,
+      [&](uint8_t* st, int64_t tile) { issue_tile<BITS, W, E, NF>(TL{st}, farr, rp, tile, nsc, t); },
+      [&](uint8_t* st, int64_t tile) { body(TL{st}, tile * TL::T + int64_t(t) * E); });
   if (ntiles * TL::T < n && blockIdx.x == ntiles % gridDim.x) {
     const int64_t e0 = ntiles * TL::T + int64_t(t) * E;
     if (e0 < n) tail(e0);
