@@ -58,6 +58,9 @@ def _load():
             lib.oracle_adam_step.argtypes = [i32, i32, vp, vp, i32, i64, i64, vp, vp, vp,
                                              f32, f32, f32, f32, f32, i32, i32, i64]
             lib.oracle_adam_step.restype = None
+            lib.oracle_compress_e8.argtypes = [i32, i32, i32, f32, f32, f32, i64,
+                                               vp, i32, vp, vp, i64, i64, vp, vp, i64, i64]
+            lib.oracle_compress_e8.restype = None
             _lib = lib
     return _lib
 
@@ -123,6 +126,39 @@ def compress(grad: np.ndarray, err: np.ndarray, step: int, *, bits: int, block: 
     def fn(b0, b1):
         lib.oracle_compress(bits, block, int(fixed), fs, float(beta), float(kappa), int(reset_period),
                             gp, is_bf16, ep, n, int(step), cp, sp, b0, b1)
+
+    if nb:
+        _run(fn, _ranges(nb, threads))
+    return codes, scales
+
+
+def compress_e8(grad: np.ndarray, err_codes: np.ndarray, err_steps: np.ndarray, step: int, *, bits: int,
+                block: int, beta: float, kappa: float, reset_period: int = 0, fixed_scale: float | None = None,
+                threads: int = 1, codes: np.ndarray | None = None, scales: np.ndarray | None = None):
+    """LoCo sender step with the error stored as int8 codes + per-block step (§3.2 Eqn 7).
+
+    err_codes (int8 [n]) and err_steps (float32 [nb]) are UPDATED IN PLACE; start from zeros.
+    Returns (codes uint8 [code_bytes], scales float32 [nb]).
+    """
+    lib = _load()
+    n = grad.size
+    nb = num_blocks(n, block)
+    assert err_codes.dtype == np.int8 and err_codes.size == n
+    assert err_steps.dtype == np.float32 and err_steps.size == nb
+    is_bf16 = 1 if grad.dtype == np.uint16 else 0
+    if not is_bf16:
+        assert grad.dtype == np.float32
+    if codes is None:
+        codes = np.zeros(code_bytes(n, bits, block), dtype=np.uint8)
+    if scales is None:
+        scales = np.zeros(nb, dtype=np.float32)
+    fixed = fixed_scale is not None
+    fs = float(fixed_scale) if fixed else 0.0
+    gp, qp, sp_, cp, scp = _ptr(grad), _ptr(err_codes), _ptr(err_steps), _ptr(codes), _ptr(scales)
+
+    def fn(b0, b1):
+        lib.oracle_compress_e8(bits, block, int(fixed), fs, float(beta), float(kappa), int(reset_period),
+                               gp, is_bf16, qp, sp_, n, int(step), cp, scp, b0, b1)
 
     if nb:
         _run(fn, _ranges(nb, threads))

@@ -257,3 +257,92 @@ void oracle_adam_step(int bits, int block, const uint8_t* const* codes,
     v[i] = vi;
   }
 }
+
+/*
+ * Sender step with the compensation error stored in 8 bits, §3.2 Eqn (7) as
+ * the paper states it: e_k = compressor(e~_k; s_e, 8) with s_e = kappa*s, and
+ * Eqn (2) adds back decompressor(e_{k-1}; s_e).  Per block b the error is kept
+ * as int8 codes qe and one step De_b (the decompressor multiplies by it), so
+ * the state costs one byte per element (the "additional Psi bytes" of the
+ * memory comparison accompanying Table I).
+ *
+ * Per block b, for the quant blocks [b0, b1):
+ *   e_prev_i = f32(qe_i) * De_b                     (stored state, De = 0 at start)
+ *   h_i      = g_i + e_prev_i                        (Eqn 2)
+ *   Delta_b, inv_b, q_i, d_i = f32(q_i)*Delta_b, r_i = h_i - d_i as in oracle_compress
+ *   t_i      = beta*e_prev_i + (1-beta)*r_i          (Eqn 5)
+ *   De_b'    = Delta_b / kappa ;  inv_e = kappa * inv_b   (s_e = kappa*s)
+ *   qe_i'    = Round_8-bit(t_i * inv_e)              (Eqn 7: nearest, halves to even, [-128,127])
+ *   qe_i'    = 0 every T_c steps (reset)
+ * err_codes [n] int8 and err_steps [nb] fp32 are updated in place.
+ */
+void oracle_compress_e8(int bits, int block, int fixed_mode, float fixed_scale,
+                        float beta, float kappa, int64_t reset_period,
+                        const void* grad, int grad_is_bf16, int8_t* err_codes, float* err_steps,
+                        int64_t n, int64_t step, uint8_t* codes, float* scales,
+                        int64_t b0, int64_t b1) {
+  const float qmax = (float)((1 << (bits - 1)) - 1);
+  const float one_minus_beta = 1.0f - beta;
+  const int reset = (reset_period > 0) && (step % reset_period == 0);
+  const int64_t bytes_per_block = (int64_t)block * bits / 8;
+  float h[1024], prev[1024];
+
+  for (int64_t b = b0; b < b1; ++b) {
+    const int64_t lo = b * block;
+    int64_t cnt = n - lo;
+    if (cnt > block) cnt = block;
+
+    /* Eqn (2): compensate with the decompressed 8-bit error. */
+    const float de_prev = err_steps[b];
+    for (int64_t j = 0; j < cnt; ++j) {
+      prev[j] = (float)err_codes[lo + j] * de_prev;
+      float g = grad_at(grad, grad_is_bf16, lo + j);
+      h[j] = g + prev[j];
+    }
+
+    float delta, inv;
+    if (fixed_mode) {
+      delta = 1.0f / fixed_scale;
+      inv = fixed_scale;
+    } else {
+      float amax = 0.0f;
+      for (int64_t j = 0; j < cnt; ++j) {
+        float a = fabsf(h[j]);
+        if (a > amax) amax = a;
+      }
+      if (amax == 0.0f) {
+        delta = 0.0f;
+        inv = 0.0f;
+      } else {
+        delta = amax / qmax;
+        inv = qmax / amax;
+      }
+    }
+    scales[b] = delta;
+
+    /* The 8-bit error compressor of scale s_e = kappa*s (Eqn 7). */
+    const float de_new = delta / kappa;
+    const float inv_e = kappa * inv;
+    err_steps[b] = de_new;
+
+    uint8_t* blk = codes + b * bytes_per_block;
+    for (int j = 0; j < block; ++j) {
+      if (j >= cnt) {
+        put_code(blk, bits, j, 0);
+        continue;
+      }
+      float x = h[j] * inv;
+      int q = round_pbit(x, bits);
+      put_code(blk, bits, j, q);
+      float d = (float)q * delta;
+      float r = h[j] - d;
+      float t1 = beta * prev[j];
+      float t2 = one_minus_beta * r;
+      float t = t1 + t2;
+      float xe = t * inv_e;
+      int qe = round_pbit(xe, 8);
+      if (reset) qe = 0;
+      err_codes[lo + j] = (int8_t)qe;
+    }
+  }
+}
