@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--workload", default="llama2-7b",
                     help="llama2-7b (default), tinyllama, mixtral, or flat:<log2 n> (bf16, 4-bit, block 256, W 8)")
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--error-storage", default="fp32", choices=["fp32", "int8"],
+                    help="compensation error kept in fp32 (default) or as int8 codes + per-block step")
     return ap.parse_args()
 
 
@@ -75,12 +77,12 @@ def workload(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
-def kernel_bytes(n, gsize, bits, block, W):
+def kernel_bytes(n, gsize, bits, block, W, e8=False):
     nb = -(-n // block)
     cb = nb * block * bits // 8
     sb = nb * 4
     return {
-        "compress": n * gsize + 8 * n + cb + sb,
+        "compress": n * gsize + (2 * n + 3 * sb if e8 else 8 * n) + cb + sb,
         "decode_reduce": W * (cb + sb) + 4 * n,
         "adam": W * (cb + sb) + 24 * n,
     }
@@ -109,19 +111,20 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, units: int, n_elems: int):
-    """DRAM bytes per launch from the committed ncu summary, scaled by elements;
-    None when the kernels changed since the counters were taken."""
+def ncu_traffic(kernel: str, units: int, n_elems: int, workload_name: str):
+    """DRAM bytes per launch of this kernel on this workload from the committed
+    ncu capture (profiles/ncu_traffic.json); None for another workload or when
+    the kernel sources changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_hash") != source_hash() or kernel not in d.get("kernels", {}):
+    if (d.get("source_hash") != source_hash() or d.get("workload") != workload_name
+            or d.get("n_elements") != n_elems or kernel not in d.get("kernels", {})):
         return None
-    k = d["kernels"][kernel]
-    return k["dram_bytes_per_element"] * n_elems
+    return d["kernels"][kernel]["dram_bytes"]
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -286,7 +289,7 @@ def cpu_baseline(w, S, steps, warmup):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, e, codes, scales, mean, param, m, v, world, dist, h2d, d2h):
+def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, param, m, v, world, dist, h2d, d2h):
     """The step through the public API with its inputs coming from page-locked
     host memory and its output (rank 0's packed buffer, the bytes a rank sends)
     going back to it, every step, inside the timed region.
@@ -345,7 +348,7 @@ def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, e, codes, scales, mean, param, m,
         comp.wait_event(g_done[k])
         if k >= 2:
             comp.wait_event(out_done[k - 2])   # rank 0's buffer of set k % 2 has left
-        L.loco_compress(cfg, gk, e, k + 1, ck[0], sk[0], stream=comp)
+        compress(gk, k + 1, ck[0], sk[0], stream=comp)
         c0_done[k].record(comp)
         comp.wait_event(in_done[k])            # ranks 1..W-1 arrived
         L.loco_decode_reduce(cfg, ck, sk, n, mean, stream=comp)
@@ -380,21 +383,40 @@ def run_loco(args, rank, world):
     w = workload(args.workload)
     n, bits, block, W = w.n, w.bits, w.block, w.W
     gsize = 2 if w.grad_dtype == torch.bfloat16 else 4
-    cfg = L.make_config(bits=bits, block=block, beta=0.9, err_scale_mult=4.0, reset_period=512)
+    # beta weights the previous error; the 8-bit storage needs weight on the new error (see loco.h)
+    cfg = L.make_config(bits=bits, block=block, beta=0.9 if args.error_storage == "fp32" else 0.1,
+                        err_scale_mult=4.0, reset_period=512)
     hp = L.make_adam(lr=1e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)
     nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
 
     # ---- resident buffers (setup, untimed)
+    e8 = args.error_storage == "int8"
     g = torch.empty(n, dtype=w.grad_dtype, device=dev)
-    e = torch.zeros(n, dtype=torch.float32, device=dev)
+    if e8:
+        e = (torch.zeros(n, dtype=torch.int8, device=dev), torch.zeros(nb, dtype=torch.float32, device=dev))
+    else:
+        e = torch.zeros(n, dtype=torch.float32, device=dev)
+
+    def compress(grad, step, c, sc, stream=None):
+        if e8:
+            L.loco_compress_e8(cfg, grad, e[0], e[1], step, c, sc, stream=stream)
+        else:
+            L.loco_compress(cfg, grad, e, step, c, sc, stream=stream)
+
+    def zero_error():
+        if e8:
+            e[0].zero_()
+            e[1].zero_()
+        else:
+            e.zero_()
     codes = [torch.empty(cb, dtype=torch.uint8, device=dev) for _ in range(W)]
     scales = [torch.empty(nb, dtype=torch.float32, device=dev) for _ in range(W)]
     for r in range(1, W):
         w.fill(g, wl.seed_for(7, 1, r))
-        e.zero_()
-        L.loco_compress(cfg, g, e, 1, codes[r], scales[r])
+        zero_error()
+        compress(g, 1, codes[r], scales[r])
     w.fill(g, wl.seed_for(7, 1, 0))
-    e.zero_()
+    zero_error()
     mean = torch.empty(n, dtype=torch.float32, device=dev)
     param = wl.fill_uniform(torch.empty(n, device=dev), 3, -0.02, 0.02)
     m = torch.zeros(n, device=dev)
@@ -409,7 +431,7 @@ def run_loco(args, rank, world):
         k = step_no[0]
         if ev:
             ev[0].record(stream)
-        L.loco_compress(cfg, g, e, k, codes[0], scales[0])
+        compress(g, k, codes[0], scales[0])
         if ev:
             ev[1].record(stream)
         L.loco_decode_reduce(cfg, codes, scales, n, mean)
@@ -463,7 +485,8 @@ def run_loco(args, rank, world):
         if h2d + d2h > 0.9 * free_dev:
             e2e_skip = f"second device buffer set needs {(h2d + d2h) / 1e9:.1f} GB, {free_dev / 1e9:.1f} GB free"
     if e2e_skip is None:
-        e2e = run_e2e(args, L, w, cfg, hp, n, nb, cb, g, e, codes, scales, mean, param, m, v, world, dist, h2d, d2h)
+        e2e = run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, param, m, v, world, dist,
+                      h2d, d2h)
 
     units_step = sum(grad_units(n, gsize, W).values())
     t_ms = total_ms / args.steps
@@ -477,13 +500,13 @@ def run_loco(args, rank, world):
         return None
 
     hbm, hbm_kind = peaks()
-    kb = kernel_bytes(n, gsize, bits, block, W)
+    kb = kernel_bytes(n, gsize, bits, block, W, e8)
     roof = {}
     for k, ms in per_kernel.items():
         ach = kb[k] / (ms * 1e-3) / 1e9
         roof[k] = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                    "frac": round(ach / hbm, 4), "ms": round(ms, 4),
-                   "traffic": ncu_traffic(k, kb[k], n), "algorithmic_bytes": kb[k],
+                   "traffic": ncu_traffic(k, kb[k], n, w.name) if not e8 else None, "algorithmic_bytes": kb[k],
                    "grad_GBps": round(grad_units(n, gsize, W)[k] / (ms * 1e-3) / 1e9, 1),
                    "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured" else
                    "fallback"}
@@ -494,8 +517,9 @@ def run_loco(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(t_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "n_elements": n, "grad_dtype": "bf16" if gsize == 2 else "fp32",
-                   "bits": bits, "block": block, "W": W, "beta": 0.9, "kappa": 4.0,
-                   "step": "loco_compress(rank 0) + loco_decode_reduce(W) + loco_adam_step(W)",
+                   "bits": bits, "block": block, "W": W, "beta": cfg.beta, "kappa": 4.0,
+                   "error_storage": args.error_storage,
+                   "step": ("loco_compress_e8" if e8 else "loco_compress") + "(rank 0) + loco_decode_reduce(W) + loco_adam_step(W)",
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU, W ranks simulated in HBM"},
         "roofline": dict(roof[dominant], kernel=dominant),

@@ -180,8 +180,15 @@ const char* loco_status_string(loco_status s) {
 
 const char* loco_last_error(void) { return g_last_error; }
 
-loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad_dtype, float* err, int64_t n,
-                          int64_t step, uint8_t* codes, float* scales, loco_stream_t stream) {
+}  // extern "C"
+
+namespace loco {
+
+// Shared by loco_compress and loco_compress_e8: exactly one of err and
+// err_codes is non-null.
+static loco_status compress_common(const loco_config* cfg, const void* grad, int32_t grad_dtype, float* err,
+                                   int8_t* err_codes, float* err_steps, int64_t n, int64_t step, uint8_t* codes,
+                                   float* scales, loco_stream_t stream) {
   if (cfg == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg is NULL");
   loco_status st = check_layout(cfg->bits, cfg->block);
   if (st != LOCO_OK) return st;
@@ -199,20 +206,27 @@ loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad
   if (step < 1) return fail(LOCO_ERR_INVALID_ARG, "step = %lld (1-based)", (long long)step);
   if (n == 0) return LOCO_OK;
 
+  const bool e8 = err_codes != nullptr || err_steps != nullptr;
   const size_t gbytes = size_t(n) * (grad_dtype == LOCO_BF16 ? 2 : 4);
-  const size_t ebytes = size_t(n) * 4;
   const size_t cbytes = size_t(loco_code_bytes(n, cfg->bits, cfg->block));
   const size_t sbytes = size_t(loco_num_blocks(n, cfg->block)) * 4;
-  const BufCheck bufs[4] = {{grad, gbytes, 16, "grad"}, {err, ebytes, 16, "err"}, {codes, cbytes, 16, "codes"},
-                            {scales, sbytes, 4, "scales"}};
-  if ((st = check_buffers(bufs, 4)) != LOCO_OK) return st;
-  if (overlap(grad, gbytes, err, ebytes) || overlap(grad, gbytes, codes, cbytes) || overlap(grad, gbytes, scales, sbytes) ||
-      overlap(err, ebytes, codes, cbytes) || overlap(err, ebytes, scales, sbytes) || overlap(codes, cbytes, scales, sbytes))
-    return fail(LOCO_ERR_INVALID_ARG, "grad, err, codes and scales must not overlap");
+  const size_t ebytes = e8 ? size_t(n) : size_t(n) * 4;
+  const void* ebuf = e8 ? static_cast<const void*>(err_codes) : static_cast<const void*>(err);
+  BufCheck bufs[5] = {{grad, gbytes, 16, "grad"}, {ebuf, ebytes, 16, e8 ? "err_codes" : "err"},
+                      {codes, cbytes, 16, "codes"}, {scales, sbytes, 4, "scales"},
+                      {err_steps, sbytes, 4, "err_steps"}};
+  if ((st = check_buffers(bufs, e8 ? 5 : 4)) != LOCO_OK) return st;
+  const int nbufs = e8 ? 5 : 4;
+  for (int i = 0; i < nbufs; ++i)
+    for (int j = i + 1; j < nbufs; ++j)
+      if (overlap(bufs[i].p, bufs[i].bytes, bufs[j].p, bufs[j].bytes))
+        return fail(LOCO_ERR_INVALID_ARG, "%s and %s overlap", bufs[i].name, bufs[j].name);
 
   CompressArgs a;
   a.grad = grad;
-  a.err = err;
+  a.err = e8 ? nullptr : err;
+  a.err_codes = e8 ? err_codes : nullptr;
+  a.err_steps = e8 ? err_steps : nullptr;
   a.codes = codes;
   a.scales = scales;
   a.n = n;
@@ -226,7 +240,26 @@ loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad
   a.one_minus_beta = 1.0f - cfg->beta;
   a.kappa = cfg->err_scale_mult;
   a.reset = cfg->reset_period > 0 && (step % cfg->reset_period) == 0;
-  return launch_result(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)), "loco_compress");
+  return launch_result(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)),
+                       e8 ? "loco_compress_e8" : "loco_compress");
+}
+
+}  // namespace loco
+
+extern "C" {
+
+loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad_dtype, float* err, int64_t n,
+                          int64_t step, uint8_t* codes, float* scales, loco_stream_t stream) {
+  if (n > 0 && err == nullptr) return fail(LOCO_ERR_INVALID_ARG, "err is NULL");
+  return compress_common(cfg, grad, grad_dtype, err, nullptr, nullptr, n, step, codes, scales, stream);
+}
+
+loco_status loco_compress_e8(const loco_config* cfg, const void* grad, int32_t grad_dtype, int8_t* err_codes,
+                             float* err_steps, int64_t n, int64_t step, uint8_t* codes, float* scales,
+                             loco_stream_t stream) {
+  if (n > 0 && (err_codes == nullptr || err_steps == nullptr))
+    return fail(LOCO_ERR_INVALID_ARG, "err_codes or err_steps is NULL");
+  return compress_common(cfg, grad, grad_dtype, nullptr, err_codes, err_steps, n, step, codes, scales, stream);
 }
 
 loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales,

@@ -12,7 +12,9 @@ constexpr int kMaxRanks = 16;
 // Everything the sender kernel needs, resolved on the host.
 struct CompressArgs {
   const void* grad;
-  float* err;
+  float* err;          // fp32 error (nullptr with 8-bit storage)
+  int8_t* err_codes;   // 8-bit error codes (nullptr with fp32 storage)
+  float* err_steps;    // per-block step of the 8-bit error codes
   uint8_t* codes;
   float* scales;
   int64_t n;

@@ -20,7 +20,7 @@ LOCO_F32, LOCO_BF16 = 0, 1
 LOCO_SCALE_ABSMAX, LOCO_SCALE_FIXED = 0, 1
 LOCO_MAX_RANKS = 16
 
-EXPORTS = ("loco_num_blocks", "loco_code_bytes", "loco_compress", "loco_decode_reduce",
+EXPORTS = ("loco_num_blocks", "loco_code_bytes", "loco_compress", "loco_compress_e8", "loco_decode_reduce",
            "loco_adam_step", "loco_status_string", "loco_last_error")
 
 
@@ -64,6 +64,8 @@ lib.loco_code_bytes.argtypes = [_i64, _i32, _i32]
 lib.loco_code_bytes.restype = _i64
 lib.loco_compress.argtypes = [ctypes.POINTER(loco_config), _vp, _i32, _vp, _i64, _i64, _vp, _vp, _vp]
 lib.loco_compress.restype = ctypes.c_int
+lib.loco_compress_e8.argtypes = [ctypes.POINTER(loco_config), _vp, _i32, _vp, _vp, _i64, _i64, _vp, _vp, _vp]
+lib.loco_compress_e8.restype = ctypes.c_int
 lib.loco_decode_reduce.argtypes = [ctypes.POINTER(loco_config), _vp, _vp, _i32, _i64, _vp, _vp]
 lib.loco_decode_reduce.restype = ctypes.c_int
 lib.loco_adam_step.argtypes = [ctypes.POINTER(loco_config), _vp, _vp, _i32, _i64, _vp, _vp, _vp,
@@ -130,6 +132,15 @@ def loco_compress(cfg: loco_config, grad, err, step: int, codes, scales, *, n: i
         n = grad.numel()
     _check(lib.loco_compress(ctypes.byref(cfg), _addr(grad), _grad_dtype(grad, grad_dtype), _addr(err),
                              n, step, _addr(codes), _addr(scales), _stream(stream)))
+
+
+def loco_compress_e8(cfg: loco_config, grad, err_codes, err_steps, step: int, codes, scales, *,
+                     n: int | None = None, grad_dtype: int | None = None, stream=None):
+    """Sender step with the error kept as int8 codes + one step per block (updated in place)."""
+    if n is None:
+        n = grad.numel()
+    _check(lib.loco_compress_e8(ctypes.byref(cfg), _addr(grad), _grad_dtype(grad, grad_dtype), _addr(err_codes),
+                                _addr(err_steps), n, step, _addr(codes), _addr(scales), _stream(stream)))
 
 
 def _rank_arrays(codes, scales):

@@ -98,7 +98,8 @@ int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block);
  * Per block b, with qmax = 2^(bits-1)-1, qmin = -2^(bits-1), k = step:
  *   h_i   = f32(g_i) + e_i                                    (Eqn 2)
  *   A_b   = max_i |h_i| over the valid elements
- *   ABSMAX: Delta_b = A_b/qmax, inv_b = qmax/A_b  (both 0 when A_b == 0)
+ *   ABSMAX: Delta_b = A_b/qmax, inv_b = qmax/A_b  (both 0 when A_b == 0, or
+ *           when qmax/A_b overflows fp32, i.e. A_b < qmax/FLT_MAX)
  *   FIXED:  Delta_b = 1/s,      inv_b = s
  *   q_i   = rint_even(clamp(h_i*inv_b, qmin, qmax))           (Eqns 1, 3)
  *   d_i   = f32(q_i)*Delta_b ;  r_i = h_i - d_i                (Eqn 4)
@@ -119,6 +120,29 @@ int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block);
 loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad_dtype,
                           float* err, int64_t n, int64_t step,
                           uint8_t* codes, float* scales, loco_stream_t stream);
+
+/*
+ * loco_compress_e8 — loco_compress with the compensation error stored in 8 bits,
+ * as the paper keeps it (§3.2 Eqn 7: e_k = compressor(e~_k; s_e, 8) with
+ * s_e = kappa*s, decompressed by Eqn 2 before it is added back): one int8 code
+ * per element plus one fp32 step per quant block instead of an fp32 error.
+ * Codes and scales are bit-identical in format to loco_compress's.
+ *
+ * Per block b (Delta_b, inv_b, q_i, d_i, r_i as in loco_compress):
+ *   e_i    = f32(qe_i) * De_b                        (stored state; zeros to start)
+ *   h_i    = f32(g_i) + e_i                           (Eqn 2)
+ *   t_i    = beta*e_i + (1-beta)*r_i                  (Eqn 5)
+ *   De_b'  = Delta_b/kappa ;  inv_e = kappa*inv_b     (s_e = kappa*s, fp32; 0 if it overflows)
+ *   qe_i'  = rint_even(clamp(t_i*inv_e, -128, 127)); 0 on a reset step (Eqn 7)
+ * err_codes [n] device int8, in/out (16-byte aligned).
+ * err_steps [nb] device fp32, in/out (the De_b; zeros to start).
+ * With s_e = 4s..6s the new contribution (1-beta)*r must exceed half a step
+ * Delta/(2*kappa) to be stored at all, so beta (weight of the previous error)
+ * should be well below 1 with this storage.
+ */
+loco_status loco_compress_e8(const loco_config* cfg, const void* grad, int32_t grad_dtype,
+                             int8_t* err_codes, float* err_steps, int64_t n, int64_t step,
+                             uint8_t* codes, float* scales, loco_stream_t stream);
 
 /*
  * loco_decode_reduce — receiver side: decode W ranks' packed buckets and

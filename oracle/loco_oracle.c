@@ -117,12 +117,14 @@ void oracle_compress(int bits, int block, int fixed_mode, float fixed_scale,
         float a = fabsf(h[j]);
         if (a > amax) amax = a;
       }
-      if (amax == 0.0f) {
+      inv = (amax == 0.0f) ? 0.0f : qmax / amax;
+      if (amax == 0.0f || isinf(inv)) {
+        /* An all-zero block, or one so small that s = qmax/A_b overflows fp32
+         * (A_b < qmax/FLT_MAX): no code can represent it; step and inverse 0. */
         delta = 0.0f;
         inv = 0.0f;
       } else {
         delta = amax / qmax;
-        inv = qmax / amax;
       }
     }
     scales[b] = delta;
@@ -310,19 +312,21 @@ void oracle_compress_e8(int bits, int block, int fixed_mode, float fixed_scale,
         float a = fabsf(h[j]);
         if (a > amax) amax = a;
       }
-      if (amax == 0.0f) {
+      inv = (amax == 0.0f) ? 0.0f : qmax / amax;
+      if (amax == 0.0f || isinf(inv)) {
         delta = 0.0f;
         inv = 0.0f;
       } else {
         delta = amax / qmax;
-        inv = qmax / amax;
       }
     }
     scales[b] = delta;
 
-    /* The 8-bit error compressor of scale s_e = kappa*s (Eqn 7). */
+    /* The 8-bit error compressor of scale s_e = kappa*s (Eqn 7); an s_e that
+     * overflows fp32 stores code 0, like a zero step. */
     const float de_new = delta / kappa;
-    const float inv_e = kappa * inv;
+    float inv_e = kappa * inv;
+    if (isinf(inv_e)) inv_e = 0.0f;
     err_steps[b] = de_new;
 
     uint8_t* blk = codes + b * bytes_per_block;

@@ -461,3 +461,33 @@ def test_adam_first_step_is_sign_descent():
                      beta2=0.999, eps=eps)
     want = 1.0 - lr * g / (np.abs(g) + eps)
     np.testing.assert_allclose(p, want, rtol=0, atol=4e-7)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_tiny_block_whose_inverse_step_overflows(bits):
+    """A block with 0 < A_b < qmax/FLT_MAX: s = qmax/A_b is not representable in
+    fp32, so the block is treated like an all-zero block: step 0, codes 0, and the
+    error range of that zero step (Eqn 7) is {0}, so the stored error is zero.
+    Just above the threshold the block quantises normally."""
+    qmax = QMAX[bits]
+    fmax = float(np.finfo(np.float32).max)
+    thresh = qmax / fmax
+    block = 64
+    tiny = np.float32(thresh * 0.5)
+    g = np.zeros(2 * block, dtype=np.float32)
+    g[:block:3] = tiny
+    g[1:block:5] = -tiny
+    big = np.float32(thresh * 4)
+    g[block:] = big
+    err = np.zeros(2 * block, dtype=np.float32)
+    codes, scales = oracle.compress(g, err, 1, bits=bits, block=block, beta=0.0, kappa=4.0)
+    assert scales[0] == 0 and not codes[:block * bits // 8].any()
+    assert np.all(err[:block] == 0)
+    assert scales[1] > 0
+    q = unpack_codes(codes, bits, 2 * block)
+    assert np.all(q[block:] == qmax)
+    qe = np.zeros(2 * block, dtype=np.int8)
+    de = np.zeros(2, dtype=np.float32)
+    c8, s8 = oracle.compress_e8(g, qe, de, 1, bits=bits, block=block, beta=0.0, kappa=4.0)
+    assert np.array_equal(c8, codes) and np.array_equal(s8, scales)
+    assert not qe[:block].any()

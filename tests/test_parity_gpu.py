@@ -264,3 +264,89 @@ def test_empty_and_errors(L):
     # nothing was launched by the rejected calls, and the stream is still healthy
     torch.cuda.synchronize()
     assert not err.any()
+
+
+def _compress_e8_both(L, cfg_kw, n, dtype, steps, seed, fixed_scale=None):
+    bits, block = cfg_kw["bits"], cfg_kw["block"]
+    cfg = L.make_config(fixed_scale=fixed_scale, **cfg_kw)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    qe = Guarded(n, torch.int8)
+    qe.view().zero_()
+    de = Guarded(4 * nb, torch.float32)
+    de.view().zero_()
+    codes, scales = Guarded(cb), Guarded(4 * nb, torch.float32)
+    qe_h = np.zeros(n, dtype=np.int8)
+    de_h = np.zeros(nb, dtype=np.float32)
+    okw = dict(bits=bits, block=block, beta=cfg_kw["beta"], kappa=cfg_kw["err_scale_mult"],
+               reset_period=cfg_kw["reset_period"], fixed_scale=fixed_scale)
+    for step in range(1, steps + 1):
+        g = _grad(n, dtype, seed + 1000 * step)
+        L.loco_compress_e8(cfg, g, qe.view(), de.view(), step, codes.view(), scales.view())
+        oc, os_ = oracle.compress_e8(grad_to_np(g), qe_h, de_h, step, **okw)
+        torch.cuda.synchronize()
+        tag = f"e8 n={n} bits={bits} block={block} {dtype} step={step}"
+        assert_bits_equal(codes.view().cpu().numpy(), oc, "codes " + tag)
+        assert_bits_equal(scales.view().cpu().numpy(), os_, "scales " + tag)
+        assert_bits_equal(qe.view().cpu().numpy(), qe_h, "err codes " + tag)
+        assert_bits_equal(de.view().cpu().numpy(), de_h, "err steps " + tag)
+        assert qe.intact() and de.intact() and codes.intact() and scales.intact(), "guard bytes " + tag
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("block", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_compress_e8_parity_small(L, bits, block, dtype):
+    for i, n in enumerate(SIZES):
+        _compress_e8_both(L, dict(bits=bits, block=block, beta=0.1, err_scale_mult=4.0, reset_period=3),
+                          n, dtype, 4, 500 + 100 * i + bits + block)
+
+
+@pytest.mark.parametrize("beta,kappa", [(0.0, 4.0), (0.5, 6.0), (0.9, 4.0), (1.0, 4.0)])
+def test_compress_e8_parity_beta_kappa(L, beta, kappa):
+    _compress_e8_both(L, dict(bits=4, block=256, beta=beta, err_scale_mult=kappa, reset_period=0),
+                      70_001, torch.bfloat16, 4, 9)
+
+
+@pytest.mark.parametrize("s", [2.0 ** 19, 2.0 ** 17])
+def test_compress_e8_parity_fixed_scale(L, s):
+    _compress_e8_both(L, dict(bits=4, block=128, beta=0.5, err_scale_mult=6.0, reset_period=2),
+                      30_003, torch.float32, 4, 13, fixed_scale=s)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_compress_tiny_blocks(L, bits):
+    """Blocks whose absmax sits around qmax/FLT_MAX (the inverse step overflows
+    fp32 below it), mixed with normal blocks, through both error storages."""
+    qmax = 7 if bits == 4 else 127
+    thresh = qmax / float(np.finfo(np.float32).max)
+    block, nblk = 64, 12
+    n = block * nblk - 5
+    gh = np.zeros(n, dtype=np.float32)
+    rng = np.random.default_rng(bits)
+    for b in range(nblk):
+        lo, hi = b * block, min((b + 1) * block, n)
+        scale = thresh * (0.25, 0.5, 0.999, 1.001, 2.0, 1e30)[b % 6]
+        gh[lo:hi] = (rng.uniform(-1, 1, hi - lo) * scale).astype(np.float32)
+    g = torch.from_numpy(gh).to(DEV)
+    cfg = L.make_config(bits=bits, block=block, beta=0.5)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    e = torch.zeros(n, device=DEV)
+    qe = torch.zeros(n, dtype=torch.int8, device=DEV)
+    de = torch.zeros(nb, device=DEV)
+    c, s = torch.empty(cb, dtype=torch.uint8, device=DEV), torch.empty(nb, device=DEV)
+    c8, s8 = torch.empty(cb, dtype=torch.uint8, device=DEV), torch.empty(nb, device=DEV)
+    e_h = np.zeros(n, np.float32)
+    qe_h, de_h = np.zeros(n, np.int8), np.zeros(nb, np.float32)
+    for step in (1, 2):
+        L.loco_compress(cfg, g, e, step, c, s)
+        L.loco_compress_e8(cfg, g, qe, de, step, c8, s8)
+        oc, os_ = oracle.compress(gh, e_h, step, bits=bits, block=block, beta=0.5, kappa=4.0)
+        oc8, os8 = oracle.compress_e8(gh, qe_h, de_h, step, bits=bits, block=block, beta=0.5, kappa=4.0)
+        torch.cuda.synchronize()
+        assert_bits_equal(c.cpu().numpy(), oc, "codes")
+        assert_bits_equal(s.cpu().numpy(), os_, "scales")
+        assert_bits_equal(e.cpu().numpy(), e_h, "err")
+        assert_bits_equal(c8.cpu().numpy(), oc8, "e8 codes")
+        assert_bits_equal(s8.cpu().numpy(), os8, "e8 scales")
+        assert_bits_equal(qe.cpu().numpy(), qe_h, "e8 err codes")
+        assert_bits_equal(de.cpu().numpy(), de_h, "e8 err steps")

@@ -229,3 +229,30 @@ def test_sweep_sizes_full_compare(L, log2n):
                         om = oracle.decode_reduce([oc] * W, [os_] * W, n, bits=bits, block=block, threads=8)
                         torch.cuda.synchronize()
                         assert_bits_equal(mean.cpu().numpy(), om, f"mean W={W} " + tag)
+
+
+def test_llama2_7b_fullsize_e8(L):
+    """The 7B bucket with the 8-bit compensation-error storage, two steps from zero state."""
+    w = W_().LLAMA2_7B
+    n, bits, block = w.n, w.bits, w.block
+    cfg = L.make_config(bits=bits, block=block, beta=0.1, err_scale_mult=4.0, reset_period=512)
+    okw = dict(bits=bits, block=block, beta=0.1, kappa=4.0, reset_period=512)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    g = torch.empty(n, dtype=w.grad_dtype, device=DEV)
+    qe = torch.zeros(n, dtype=torch.int8, device=DEV)
+    de = torch.zeros(nb, dtype=torch.float32, device=DEV)
+    codes = torch.empty(cb, dtype=torch.uint8, device=DEV)
+    scales = torch.empty(nb, dtype=torch.float32, device=DEV)
+    for k in (1, 2):
+        s = Sampler(n, block, 300 + k)
+        w.fill(g, W_().seed_for(7, k, 0))
+        g_h = grad_to_np(s.grab(g))
+        qe_h = s.grab(qe).numpy().copy()
+        de_h = scale_rows(de, s.ids).copy()
+        L.loco_compress_e8(cfg, g, qe, de, k, codes, scales)
+        oc, os_ = oracle.compress_e8(g_h, qe_h, de_h, k, **okw)
+        torch.cuda.synchronize()
+        assert_bits_equal(code_rows(codes, s.ids, block, bits), oc, f"e8 codes step {k}")
+        assert_bits_equal(scale_rows(scales, s.ids), os_, f"e8 scales step {k}")
+        assert_bits_equal(s.grab(qe).numpy(), qe_h, f"e8 err codes step {k}")
+        assert_bits_equal(scale_rows(de, s.ids), de_h, f"e8 err steps step {k}")
