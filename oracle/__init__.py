@@ -55,12 +55,14 @@ def _load():
             lib.oracle_compress.restype = None
             lib.oracle_decode_reduce.argtypes = [i32, i32, vp, vp, i32, i64, i64, vp, vp]
             lib.oracle_decode_reduce.restype = None
-            lib.oracle_adam_step.argtypes = [i32, i32, vp, vp, i32, i64, i64, vp, vp, vp,
+            lib.oracle_adam_step.argtypes = [i32, i32, vp, vp, i32, i64, i64, vp, vp, vp, vp,
                                              f32, f32, f32, f32, f32, i32, i32, i64]
             lib.oracle_adam_step.restype = None
             lib.oracle_compress_e8.argtypes = [i32, i32, i32, f32, f32, f32, i64,
                                                vp, i32, vp, vp, i64, i64, vp, vp, i64, i64]
             lib.oracle_compress_e8.restype = None
+            lib.oracle_sgd_step.argtypes = [i32, i32, vp, vp, i32, i64, i64, vp, vp, f32]
+            lib.oracle_sgd_step.restype = None
             _lib = lib
     return _lib
 
@@ -193,20 +195,44 @@ def decode_reduce(codes_list, scales_list, n: int, *, bits: int, block: int,
 def adam_step(codes_list, scales_list, n: int, param: np.ndarray, m: np.ndarray, v: np.ndarray,
               t: int, *, bits: int, block: int, lr: float, beta1: float, beta2: float,
               eps: float, weight_decay: float = 0.0, bias_correction: bool = True,
-              eps_inside_sqrt: bool = False, threads: int = 1):
-    """Eqn 8 average fed to one Adam(W) step (§4 Eqn 9); param, m, v updated in place."""
+              eps_inside_sqrt: bool = False, param_bf16: np.ndarray | None = None, threads: int = 1):
+    """Eqn 8 average fed to one Adam(W) step (§4 Eqn 9); param, m, v updated in place.
+    param_bf16 (uint16 [n], optional) receives the updated param rounded to bf16."""
     lib = _load()
     W = len(codes_list)
     for a in (param, m, v):
         assert a.dtype == np.float32 and a.size == n
+    if param_bf16 is not None:
+        assert param_bf16.dtype == np.uint16 and param_bf16.size == n
     cpa = _ptr_array(codes_list, ctypes.c_uint8)
     spa = _ptr_array(scales_list, ctypes.c_float)
     pp, mp, vp = _ptr(param), _ptr(m), _ptr(v)
+    bp = _ptr(param_bf16) if param_bf16 is not None else None
 
     def fn(i0, i1):
-        lib.oracle_adam_step(bits, block, cpa, spa, W, i0, i1, pp, mp, vp,
+        lib.oracle_adam_step(bits, block, cpa, spa, W, i0, i1, pp, mp, vp, bp,
                              float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
                              int(bias_correction), int(eps_inside_sqrt), int(t))
+
+    if n:
+        _run(fn, _ranges(n, threads))
+
+
+def sgd_step(codes_list, scales_list, n: int, param: np.ndarray, *, bits: int, block: int, lr: float,
+             param_bf16: np.ndarray | None = None, threads: int = 1):
+    """Eqn 8 average fed to one LoCo-SGD step (§4): param -= lr * g~ (in place)."""
+    lib = _load()
+    W = len(codes_list)
+    assert param.dtype == np.float32 and param.size == n
+    if param_bf16 is not None:
+        assert param_bf16.dtype == np.uint16 and param_bf16.size == n
+    cpa = _ptr_array(codes_list, ctypes.c_uint8)
+    spa = _ptr_array(scales_list, ctypes.c_float)
+    pp = _ptr(param)
+    bp = _ptr(param_bf16) if param_bf16 is not None else None
+
+    def fn(i0, i1):
+        lib.oracle_sgd_step(bits, block, cpa, spa, W, i0, i1, pp, bp, float(lr))
 
     if n:
         _run(fn, _ranges(n, threads))

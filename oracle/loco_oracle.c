@@ -28,6 +28,16 @@ static float bf16_bits_to_f32(uint16_t b) {
   return f;
 }
 
+/* fp32 -> bf16, round to nearest, halves to even: keep the high 16 bits of
+ * u + 0x7FFF + (bit 16 of u).  NaN keeps its sign and becomes a quiet NaN. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x0040u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
 /* Round_p-bit of Eqn (1): nearest integer, halves to even (the rounding of
  * torch.round, "the default one in PyTorch", §3.1), saturated to
  * [-2^(p-1), 2^(p-1)-1].  Saturating first and rounding second gives the same
@@ -206,7 +216,7 @@ void oracle_decode_reduce(int bits, int block, const uint8_t* const* codes,
  */
 void oracle_adam_step(int bits, int block, const uint8_t* const* codes,
                       const float* const* scales, int W, int64_t i0, int64_t i1,
-                      float* param, float* m, float* v,
+                      float* param, float* m, float* v, uint16_t* param_bf16,
                       float lr, float beta1, float beta2, float eps, float wd,
                       int bias_correction, int eps_inside_sqrt, int64_t t) {
   const int64_t bytes_per_block = (int64_t)block * bits / 8;
@@ -257,6 +267,36 @@ void oracle_adam_step(int bits, int block, const uint8_t* const* codes,
     param[i] = p;
     m[i] = mi;
     v[i] = vi;
+    if (param_bf16) param_bf16[i] = f32_to_bf16_rne(p);
+  }
+}
+
+/*
+ * Receiver step fused with LoCo-SGD, §4: theta_{k+1} = theta_k - eta * g~_k with
+ * g~ the average of Eqn (8) (formed as in oracle_decode_reduce), for elements
+ * [i0, i1).  If param_bf16 is not NULL it receives the updated parameter
+ * rounded to bf16 (nearest, halves to even): the 16-bit copy that the sharded
+ * data-parallel setting gathers (the 16-bit parameters of the Table I
+ * comparison).
+ */
+void oracle_sgd_step(int bits, int block, const uint8_t* const* codes,
+                     const float* const* scales, int W, int64_t i0, int64_t i1,
+                     float* param, uint16_t* param_bf16, float lr) {
+  const int64_t bytes_per_block = (int64_t)block * bits / 8;
+  for (int64_t i = i0; i < i1; ++i) {
+    const int64_t b = i / block;
+    const int j = (int)(i % block);
+    float acc = 0.0f;
+    for (int w = 0; w < W; ++w) {
+      int q = get_code(codes[w] + b * bytes_per_block, bits, j);
+      float d = (float)q * scales[w][b];
+      acc = (w == 0) ? d : acc + d;
+    }
+    float g = acc / (float)W;
+    float step = lr * g;
+    float p = param[i] - step;
+    param[i] = p;
+    if (param_bf16) param_bf16[i] = f32_to_bf16_rne(p);
   }
 }
 

@@ -491,3 +491,46 @@ def test_tiny_block_whose_inverse_step_overflows(bits):
     c8, s8 = oracle.compress_e8(g, qe, de, 1, bits=bits, block=block, beta=0.0, kappa=4.0)
     assert np.array_equal(c8, codes) and np.array_equal(s8, scales)
     assert not qe[:block].any()
+
+
+# ---------------------------------------------------------------- §4 SGD and the bf16 parameter copy
+
+def test_bf16_rounding_matches_torch():
+    """The oracle's fp32 -> bf16 rounding (nearest, halves to even) against
+    torch's conversion, on random values, exact ties and overflow to inf."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(30)
+    x = (rng.standard_normal(20000) * 10.0 ** rng.uniform(-30, 30, 20000)).astype(np.float32)
+    u = x.view(np.uint32)
+    ties = ((u & 0xFFFF0000) | 0x8000).view(np.float32)      # exactly halfway
+    big = np.array([3.3e38, -3.39e38, np.finfo(np.float32).max], dtype=np.float32)
+    vals = np.concatenate([x, ties, big, np.float32([0.0, -0.0, 1e-40, -1e-45])])
+    n = vals.size
+    codes = [np.zeros(oracle.code_bytes(n, 8, 64), dtype=np.uint8)]
+    scales = [np.zeros(oracle.num_blocks(n, 64), dtype=np.float32)]
+    p = vals.copy()
+    out = np.zeros(n, dtype=np.uint16)
+    oracle.sgd_step(codes, scales, n, p, bits=8, block=64, lr=1.0, param_bf16=out)  # g~ = 0: p unchanged
+    want = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(p, vals)
+    assert np.array_equal(out, want)
+
+
+def test_sgd_step_closed_form():
+    """W = 1, dyadic codes and step: g~ = q*Delta exactly and theta - lr*g~ is exact."""
+    n, bits, block = 64, 4, 64
+    u = 2.0 ** -10
+    q = np.array([4, -4, 2, -1, 7, -8, 0, 3] * 8)
+    codes = np.zeros(32, dtype=np.uint8)
+    for j in range(0, 64, 2):
+        codes[j // 2] = (q[j] & 0xF) | ((q[j + 1] & 0xF) << 4)
+    scales = np.array([u], dtype=np.float32)
+    p0 = (np.arange(n, dtype=np.float32) - 32) * np.float32(0.25)
+    p = p0.copy()
+    out = np.zeros(n, dtype=np.uint16)
+    oracle.sgd_step([codes], [scales], n, p, bits=bits, block=block, lr=2.0 ** -3, param_bf16=out)
+    want = p0.astype(np.float64) - 2.0 ** -3 * q * u
+    assert np.array_equal(p.astype(np.float64), want)
+    # decode_reduce gives the same g~
+    g = oracle.decode_reduce([codes], [scales], n, bits=bits, block=block)
+    assert np.array_equal(p, (p0 - np.float32(2.0 ** -3) * g).astype(np.float32))
