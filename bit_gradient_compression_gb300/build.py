@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libloco.so")
 
-SOURCES = ["abi.cu", "compress.cu", "reduce.cu"]
+SOURCES = ["abi.cu", "compress.cu", "decode_reduce.cu", "adam.cu", "sgd.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere; every fp32 product and sum

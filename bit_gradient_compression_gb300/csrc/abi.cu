@@ -291,15 +291,48 @@ loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* cod
   return launch_result(launch_decode_reduce(a, reinterpret_cast<cudaStream_t>(stream)), "loco_decode_reduce");
 }
 
-loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales, int32_t W,
-                           int64_t n, float* param, float* m, float* v, const loco_adam_hparams* hp, int64_t t,
-                           loco_stream_t stream) {
-  if (cfg == nullptr || hp == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg or hp is NULL");
+}  // extern "C"
+
+namespace loco {
+
+// Shared checks of the fused optimizer entry points: layout, ranks, the
+// param/state buffers and their overlaps.  fbufs lists param (+ m, v).
+static loco_status check_update(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales,
+                                int32_t W, int64_t n, RankPtrs* ranks, const BufCheck* fbufs, int nf,
+                                uint16_t* param_bf16) {
+  loco_status st;
+  BufCheck bufs[2 * kMaxRanks + 4];
+  int nbuf = 0;
+  if ((st = check_ranks(cfg, codes, scales, W, n, ranks, bufs, &nbuf)) != LOCO_OK) return st;
+  const int nranks = nbuf;
+  for (int i = 0; i < nf; ++i) bufs[nbuf++] = fbufs[i];
+  if (param_bf16 != nullptr) bufs[nbuf++] = BufCheck{param_bf16, size_t(n) * 2, 16, "param_bf16"};
+  if ((st = check_buffers(bufs, nbuf)) != LOCO_OK) return st;
+  // Outputs (after the ranks' read-only inputs, which may alias each other)
+  // must not overlap any other buffer.
+  for (int i = nranks; i < nbuf; ++i)
+    for (int j = 0; j < nbuf; ++j)
+      if (j != i && overlap(bufs[i].p, bufs[i].bytes, bufs[j].p, bufs[j].bytes))
+        return fail(LOCO_ERR_INVALID_ARG, "%s overlaps %s", bufs[i].name, bufs[j].name);
+  return LOCO_OK;
+}
+
+static loco_status check_common(const loco_config* cfg, int32_t W, int64_t n) {
+  if (cfg == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg is NULL");
   loco_status st = check_layout(cfg->bits, cfg->block);
   if (st != LOCO_OK) return st;
   if (n < 0) return fail(LOCO_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
   if (W < 1) return fail(LOCO_ERR_INVALID_ARG, "W = %d (need >= 1)", W);
   if (W > kMaxRanks) return fail(LOCO_ERR_UNSUPPORTED, "W = %d (at most %d)", W, kMaxRanks);
+  return LOCO_OK;
+}
+
+static loco_status adam_common(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales,
+                               int32_t W, int64_t n, float* param, float* m, float* v, uint16_t* param_bf16,
+                               const loco_adam_hparams* hp, int64_t t, loco_stream_t stream) {
+  if (hp == nullptr) return fail(LOCO_ERR_INVALID_ARG, "hp is NULL");
+  loco_status st = check_common(cfg, W, n);
+  if (st != LOCO_OK) return st;
   if (t < 1) return fail(LOCO_ERR_INVALID_ARG, "t = %lld (1-based)", (long long)t);
   if (!isfinite(hp->lr) || !isfinite(hp->eps) || !isfinite(hp->weight_decay) || hp->eps < 0.0f)
     return fail(LOCO_ERR_INVALID_ARG, "lr, eps, weight_decay must be finite and eps >= 0");
@@ -307,22 +340,9 @@ loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes, 
     return fail(LOCO_ERR_INVALID_ARG, "beta1 = %g, beta2 = %g must lie in [0, 1)", hp->beta1, hp->beta2);
   if (n == 0) return LOCO_OK;
   AdamArgs a;
-  BufCheck bufs[2 * kMaxRanks + 3];
-  int nbuf = 0;
-  if ((st = check_ranks(cfg, codes, scales, W, n, &a.ranks, bufs, &nbuf)) != LOCO_OK) return st;
   const size_t fbytes = size_t(n) * 4;
-  bufs[nbuf++] = BufCheck{param, fbytes, 16, "param"};
-  bufs[nbuf++] = BufCheck{m, fbytes, 16, "m"};
-  bufs[nbuf++] = BufCheck{v, fbytes, 16, "v"};
-  if ((st = check_buffers(bufs, nbuf)) != LOCO_OK) return st;
-  if (overlap(param, fbytes, m, fbytes) || overlap(param, fbytes, v, fbytes) || overlap(m, fbytes, v, fbytes))
-    return fail(LOCO_ERR_INVALID_ARG, "param, m and v must not overlap");
-  const size_t cbytes = size_t(loco_code_bytes(n, cfg->bits, cfg->block));
-  const size_t sbytes = size_t(loco_num_blocks(n, cfg->block)) * 4;
-  for (int w = 0; w < W; ++w)
-    for (const float* out : {static_cast<const float*>(param), static_cast<const float*>(m), static_cast<const float*>(v)})
-      if (overlap(out, fbytes, codes[w], cbytes) || overlap(out, fbytes, scales[w], sbytes))
-        return fail(LOCO_ERR_INVALID_ARG, "param/m/v overlap the inputs of rank %d", w);
+  const BufCheck fb[3] = {{param, fbytes, 16, "param"}, {m, fbytes, 16, "m"}, {v, fbytes, 16, "v"}};
+  if ((st = check_update(cfg, codes, scales, W, n, &a.ranks, fb, 3, param_bf16)) != LOCO_OK) return st;
   a.W = W;
   a.n = n;
   a.bits = cfg->bits;
@@ -330,6 +350,7 @@ loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes, 
   a.param = param;
   a.m = m;
   a.v = v;
+  a.param_bf16 = param_bf16;
   a.beta1 = hp->beta1;
   a.beta2 = hp->beta2;
   a.one_minus_beta1 = 1.0f - hp->beta1;
@@ -345,7 +366,44 @@ loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes, 
   }
   a.eps = hp->eps;
   a.eps_inside_sqrt = hp->eps_inside_sqrt != 0;
-  return launch_result(launch_adam(a, reinterpret_cast<cudaStream_t>(stream)), "loco_adam_step");
+  return launch_result(launch_adam(a, reinterpret_cast<cudaStream_t>(stream)),
+                       param_bf16 ? "loco_adam_step_bf16" : "loco_adam_step");
+}
+
+}  // namespace loco
+
+extern "C" {
+
+loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales, int32_t W,
+                           int64_t n, float* param, float* m, float* v, const loco_adam_hparams* hp, int64_t t,
+                           loco_stream_t stream) {
+  return adam_common(cfg, codes, scales, W, n, param, m, v, nullptr, hp, t, stream);
+}
+
+loco_status loco_adam_step_bf16(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales,
+                                int32_t W, int64_t n, float* param, float* m, float* v, uint16_t* param_bf16,
+                                const loco_adam_hparams* hp, int64_t t, loco_stream_t stream) {
+  if (n > 0 && param_bf16 == nullptr) return fail(LOCO_ERR_INVALID_ARG, "param_bf16 is NULL");
+  return adam_common(cfg, codes, scales, W, n, param, m, v, param_bf16, hp, t, stream);
+}
+
+loco_status loco_sgd_step(const loco_config* cfg, const uint8_t* const* codes, const float* const* scales, int32_t W,
+                          int64_t n, float* param, uint16_t* param_bf16, float lr, loco_stream_t stream) {
+  loco_status st = check_common(cfg, W, n);
+  if (st != LOCO_OK) return st;
+  if (!isfinite(lr)) return fail(LOCO_ERR_INVALID_ARG, "lr = %g must be finite", lr);
+  if (n == 0) return LOCO_OK;
+  SgdArgs a;
+  const BufCheck fb[1] = {{param, size_t(n) * 4, 16, "param"}};
+  if ((st = check_update(cfg, codes, scales, W, n, &a.ranks, fb, 1, param_bf16)) != LOCO_OK) return st;
+  a.W = W;
+  a.n = n;
+  a.bits = cfg->bits;
+  a.block = cfg->block;
+  a.param = param;
+  a.param_bf16 = param_bf16;
+  a.lr = lr;
+  return launch_result(launch_sgd(a, reinterpret_cast<cudaStream_t>(stream)), "loco_sgd_step");
 }
 
 }  // extern "C"

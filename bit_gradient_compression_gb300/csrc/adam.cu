@@ -1,0 +1,91 @@
+// Receiver average of Eqn (8) fed to one Adam(W) step (§4 Eqn 9) of "LoCo:
+// Low-Bit Communication Adaptor for Large-scale Model Training": param, m, v,
+// codes and steps staged per tile; the updated param, m, v (and optionally the
+// bf16 copy of param) stored straight from registers.
+#include "receiver_common.cuh"
+
+namespace loco {
+
+#ifndef LOCO_ADAM_ELEMS
+#define LOCO_ADAM_ELEMS(bits) 8
+#endif
+#ifndef LOCO_ADAM_STAGES
+#define LOCO_ADAM_STAGES 2
+#endif
+
+// One Adam(W) update of one element, in the order the header states.
+__device__ __forceinline__ void adam_elem(const AdamArgs& a, float g, float& p, float& m, float& v) {
+  p = __fsub_rn(p, __fmul_rn(a.lr_wd, p));
+  m = __fadd_rn(__fmul_rn(a.beta1, m), __fmul_rn(a.one_minus_beta1, g));
+  v = __fadd_rn(__fmul_rn(a.beta2, v), __fmul_rn(a.one_minus_beta2, __fmul_rn(g, g)));
+  const float den = a.eps_inside_sqrt ? __fsqrt_rn(__fadd_rn(__fmul_rn(v, a.c2), a.eps))
+                                      : __fadd_rn(__fmul_rn(__fsqrt_rn(v), a.c2), a.eps);
+  p = __fsub_rn(p, __fmul_rn(a.c1, __fdiv_rn(m, den)));
+}
+
+template <int BITS, int W, int E, int S, bool BF16OUT>
+__global__ void __launch_bounds__(kThreads) k_adam(const AdamArgs a, int log2_block) {
+  using TL = Tile<BITS, W, E, 3>;
+  const float* farr[3] = {a.param, a.m, a.v};
+  tile_pipeline<BITS, W, E, 3, S>(
+      farr, a.ranks, a.n, log2_block,
+      [&](const TL& tl, int64_t e0) {
+        const int t = threadIdx.x;
+        float p[E], m[E], v[E], g[E];
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+          const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
+          const float4 mv = reinterpret_cast<const float4*>(tl.f(1) + t * E)[q];
+          const float4 vv = reinterpret_cast<const float4*>(tl.f(2) + t * E)[q];
+          p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
+          m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
+          v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
+        }
+        tile_mean<BITS, W, E, 3>(tl, t, log2_block, g);
+#pragma unroll
+        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+        store_vec<E>(a.param, e0, a.n, true, p);
+        store_vec<E>(a.m, e0, a.n, true, m);
+        store_vec<E>(a.v, e0, a.n, true, v);
+        if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, true, p);
+      },
+      [&](int64_t e0) {
+        const bool full = e0 + E <= a.n;
+        float p[E], m[E], v[E], g[E];
+        load_vec<E>(a.param, e0, a.n, full, p);
+        load_vec<E>(a.m, e0, a.n, full, m);
+        load_vec<E>(a.v, e0, a.n, full, v);
+        decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
+#pragma unroll
+        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+        store_vec<E>(a.param, e0, a.n, full, p);
+        store_vec<E>(a.m, e0, a.n, full, m);
+        store_vec<E>(a.v, e0, a.n, full, v);
+        if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, full, p);
+      });
+}
+
+template <int BITS, bool BF16OUT>
+struct AdamLaunch {
+  template <int W>
+  struct F {
+    static cudaError_t run(const AdamArgs& a, cudaStream_t s) {
+      constexpr int E = LOCO_ADAM_ELEMS(BITS);
+      constexpr int S = fit_stages<BITS, W, E, 3>(LOCO_ADAM_STAGES);
+      constexpr size_t smem = S * Tile<BITS, W, E, 3>::kBytes;
+      static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
+      const void* fn = reinterpret_cast<const void*>(&k_adam<BITS, W, E, S, BF16OUT>);
+      static const int cap = receiver_grid(fn, smem);
+      k_adam<BITS, W, E, S, BF16OUT><<<clamp_grid(a.n, kThreads * E, cap), kThreads, smem, s>>>(a, ilog2_int(a.block));
+      return cudaGetLastError();
+    }
+  };
+};
+
+cudaError_t launch_adam(const AdamArgs& a, cudaStream_t s) {
+  if (a.param_bf16 != nullptr)
+    return a.bits == 4 ? dispatch_w<AdamLaunch<4, true>::F>(a.W, a, s) : dispatch_w<AdamLaunch<8, true>::F>(a.W, a, s);
+  return a.bits == 4 ? dispatch_w<AdamLaunch<4, false>::F>(a.W, a, s) : dispatch_w<AdamLaunch<8, false>::F>(a.W, a, s);
+}
+
+}  // namespace loco

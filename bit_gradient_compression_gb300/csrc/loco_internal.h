@@ -53,6 +53,7 @@ struct AdamArgs {
   float* param;
   float* m;
   float* v;
+  uint16_t* param_bf16;  // optional bf16 copy of the updated param (nullptr: none)
   float beta1, beta2;
   float one_minus_beta1, one_minus_beta2;
   float lr_wd;
@@ -62,9 +63,21 @@ struct AdamArgs {
   int eps_inside_sqrt;
 };
 
+struct SgdArgs {
+  RankPtrs ranks;
+  int W;
+  int64_t n;
+  int bits;
+  int block;
+  float* param;
+  uint16_t* param_bf16;  // optional bf16 copy of the updated param (nullptr: none)
+  float lr;
+};
+
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 cudaError_t launch_decode_reduce(const ReduceArgs& a, cudaStream_t s);
 cudaError_t launch_adam(const AdamArgs& a, cudaStream_t s);
+cudaError_t launch_sgd(const SgdArgs& a, cudaStream_t s);
 
 // Number of CTAs for a grid-stride kernel: resident CTAs per SM x SMs.
 int persistent_grid(const void* kernel, int threads, size_t smem_bytes = 0);

@@ -1,12 +1,16 @@
-// Receiver side of LoCo: decode W ranks' packed buckets and average them in
-// fp32 ("LoCo: Low-Bit Communication Adaptor for Large-scale Model Training",
-// §3.3 Eqn 8), optionally feeding the average straight into one Adam(W) step
-// (§4 Eqn 9) so that it never touches HBM.
+// Shared machinery of the receiver kernels of LoCo ("LoCo: Low-Bit
+// Communication Adaptor for Large-scale Model Training", §3.3 Eqn 8 and §4):
+// decode W ranks' packed buckets, average them in fp32, and either store the
+// average or feed it straight into an optimizer step without touching HBM.
 //
 // Mapping: a CTA of 256 threads consumes tiles of 256*E elements staged in
 // shared memory by a multistage cp.async pipeline (coalesced 16-byte pieces of
 // every input of the tile); thread t owns elements [t*E, t*E + E) of a tile.
 // The rank count W is a template parameter so the rank loop unrolls fully.
+#pragma once
+
+#include <cuda_bf16.h>
+
 #include "device_common.cuh"
 
 namespace loco {
@@ -128,140 +132,55 @@ __device__ __forceinline__ void tile_pipeline(const float* const* farr, const Ra
   }
 }
 
-// Receiver average (Eqn 8): codes and steps staged per tile, the mean stored
-// straight from registers.
-template <int BITS, int W, int E, int S>
-__global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, int log2_block) {
-  using TL = Tile<BITS, W, E, 0>;
-  const float* none[1] = {nullptr};
-  tile_pipeline<BITS, W, E, 0, S>(
-      none, a.ranks, a.n, log2_block,
-      [&](const TL& tl, int64_t e0) {
-        float mean[E];
-        tile_mean<BITS, W, E, 0>(tl, threadIdx.x, log2_block, mean);
-        store_vec<E>(a.mean, e0, a.n, true, mean);
-      },
-      [&](int64_t e0) {
-        float mean[E];
-        decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, mean);
-        store_vec<E>(a.mean, e0, a.n, e0 + E <= a.n, mean);
-      });
+
+// bf16 copy of E updated parameters (round to nearest even).
+template <int E>
+__device__ __forceinline__ void store_bf16(uint16_t* dst, int64_t e0, int64_t n, bool full, const float p[E]) {
+  uint32_t w[E / 2];
+#pragma unroll
+  for (int j = 0; j < E / 2; ++j)
+    w[j] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(p[2 * j]))) |
+           (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(p[2 * j + 1]))) << 16);
+  if (full) {
+#pragma unroll
+    for (int i = 0; i < E / 8; ++i)
+      st_stream(reinterpret_cast<uint4*>(dst + e0) + i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+      if (e0 + j < n) dst[e0 + j] = uint16_t(w[j / 2] >> (16 * (j & 1)));
+  }
 }
 
-// One Adam(W) update of one element, in the order the header states.
-__device__ __forceinline__ void adam_elem(const AdamArgs& a, float g, float& p, float& m, float& v) {
-  p = __fsub_rn(p, __fmul_rn(a.lr_wd, p));
-  m = __fadd_rn(__fmul_rn(a.beta1, m), __fmul_rn(a.one_minus_beta1, g));
-  v = __fadd_rn(__fmul_rn(a.beta2, v), __fmul_rn(a.one_minus_beta2, __fmul_rn(g, g)));
-  const float den = a.eps_inside_sqrt ? __fsqrt_rn(__fadd_rn(__fmul_rn(v, a.c2), a.eps))
-                                      : __fadd_rn(__fmul_rn(__fsqrt_rn(v), a.c2), a.eps);
-  p = __fsub_rn(p, __fmul_rn(a.c1, __fdiv_rn(m, den)));
-}
-
-// Receiver average fed to Adam (Eqns 8, 9): param, m, v, codes and steps
-// staged per tile; the updated param, m, v stored straight from registers.
-template <int BITS, int W, int E, int S>
-__global__ void __launch_bounds__(kThreads) k_adam(const AdamArgs a, int log2_block) {
-  using TL = Tile<BITS, W, E, 3>;
-  const float* farr[3] = {a.param, a.m, a.v};
-  tile_pipeline<BITS, W, E, 3, S>(
-      farr, a.ranks, a.n, log2_block,
-      [&](const TL& tl, int64_t e0) {
-        const int t = threadIdx.x;
-        float p[E], m[E], v[E], g[E];
-#pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-          const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
-          const float4 mv = reinterpret_cast<const float4*>(tl.f(1) + t * E)[q];
-          const float4 vv = reinterpret_cast<const float4*>(tl.f(2) + t * E)[q];
-          p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
-          m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
-          v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
-        }
-        tile_mean<BITS, W, E, 3>(tl, t, log2_block, g);
-#pragma unroll
-        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
-        store_vec<E>(a.param, e0, a.n, true, p);
-        store_vec<E>(a.m, e0, a.n, true, m);
-        store_vec<E>(a.v, e0, a.n, true, v);
-      },
-      [&](int64_t e0) {
-        const bool full = e0 + E <= a.n;
-        float p[E], m[E], v[E], g[E];
-        load_vec<E>(a.param, e0, a.n, full, p);
-        load_vec<E>(a.m, e0, a.n, full, m);
-        load_vec<E>(a.v, e0, a.n, full, v);
-        decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
-#pragma unroll
-        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
-        store_vec<E>(a.param, e0, a.n, full, p);
-        store_vec<E>(a.m, e0, a.n, full, m);
-        store_vec<E>(a.v, e0, a.n, full, v);
-      });
-}
-
-static int ilog2(int x) {
+static inline int ilog2_int(int x) {
   int r = 0;
   while ((1 << r) < x) ++r;
   return r;
 }
 
-#ifndef LOCO_REDUCE_ELEMS
-#define LOCO_REDUCE_ELEMS(bits) (64 / (bits))  // elements per thread chunk: 8 code bytes per rank
-#endif
-#ifndef LOCO_REDUCE_STAGES
-#define LOCO_REDUCE_STAGES 4
-#endif
-#ifndef LOCO_ADAM_ELEMS
-#define LOCO_ADAM_ELEMS(bits) 8
-#endif
-#ifndef LOCO_ADAM_STAGES
-#define LOCO_ADAM_STAGES 2
-#endif
-
-template <typename Args, int BITS, int W, bool ADAM>
-static cudaError_t launch_w(const Args& a, cudaStream_t s) {
-  constexpr int E = ADAM ? LOCO_ADAM_ELEMS(BITS) : LOCO_REDUCE_ELEMS(BITS);
-  constexpr int S = ADAM ? fit_stages<BITS, W, E, 3>(LOCO_ADAM_STAGES) : fit_stages<BITS, W, E, 0>(LOCO_REDUCE_STAGES);
-  constexpr size_t smem = S * (ADAM ? Tile<BITS, W, E, 3>::kBytes : Tile<BITS, W, E, 0>::kBytes);
-  static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
-  const void* fn;
-  if constexpr (ADAM)
-    fn = reinterpret_cast<const void*>(&k_adam<BITS, W, E, S>);
-  else
-    fn = reinterpret_cast<const void*>(&k_decode_reduce<BITS, W, E, S>);
-  static const int cap = [&] {
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    return persistent_grid(fn, kThreads, smem);
-  }();
-  const int64_t nchunks = (a.n + E - 1) / E;
-  const int64_t ctas_needed = (nchunks + kThreads - 1) / kThreads;
-  const int grid = int(ctas_needed < cap ? ctas_needed : cap);
-  if constexpr (ADAM)
-    k_adam<BITS, W, E, S><<<grid, kThreads, smem, s>>>(a, ilog2(a.block));
-  else
-    k_decode_reduce<BITS, W, E, S><<<grid, kThreads, smem, s>>>(a, ilog2(a.block));
-  return cudaGetLastError();
+// Resident CTAs/SM x SMs for a receiver kernel with `smem` bytes of staging,
+// computed once per kernel (static local in the caller's instantiation).
+static inline int receiver_grid(const void* fn, size_t smem) {
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  return persistent_grid(fn, kThreads, smem);
 }
 
-template <typename Args, int BITS, bool ADAM>
-static cudaError_t launch_bits(const Args& a, cudaStream_t s) {
-  switch (a.W) {
+static inline int clamp_grid(int64_t n, int elems_per_cta, int cap) {
+  const int64_t need = (n + elems_per_cta - 1) / elems_per_cta;
+  return int(need < cap ? need : cap);
+}
+
+// Dispatch of a runtime rank count to a template parameter 1..16.
+template <template <int> class F, typename... A>
+static cudaError_t dispatch_w(int W, A&&... args) {
+  switch (W) {
 #define LOCO_CASE(w) \
-  case w: return launch_w<Args, BITS, w, ADAM>(a, s);
+  case w: return F<w>::run(args...);
     LOCO_CASE(1) LOCO_CASE(2) LOCO_CASE(3) LOCO_CASE(4) LOCO_CASE(5) LOCO_CASE(6) LOCO_CASE(7) LOCO_CASE(8)
     LOCO_CASE(9) LOCO_CASE(10) LOCO_CASE(11) LOCO_CASE(12) LOCO_CASE(13) LOCO_CASE(14) LOCO_CASE(15) LOCO_CASE(16)
 #undef LOCO_CASE
   }
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_decode_reduce(const ReduceArgs& a, cudaStream_t s) {
-  return a.bits == 4 ? launch_bits<ReduceArgs, 4, false>(a, s) : launch_bits<ReduceArgs, 8, false>(a, s);
-}
-
-cudaError_t launch_adam(const AdamArgs& a, cudaStream_t s) {
-  return a.bits == 4 ? launch_bits<AdamArgs, 4, true>(a, s) : launch_bits<AdamArgs, 8, true>(a, s);
 }
 
 }  // namespace loco

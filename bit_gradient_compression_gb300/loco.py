@@ -21,7 +21,7 @@ LOCO_SCALE_ABSMAX, LOCO_SCALE_FIXED = 0, 1
 LOCO_MAX_RANKS = 16
 
 EXPORTS = ("loco_num_blocks", "loco_code_bytes", "loco_compress", "loco_compress_e8", "loco_decode_reduce",
-           "loco_adam_step", "loco_status_string", "loco_last_error")
+           "loco_adam_step", "loco_adam_step_bf16", "loco_sgd_step", "loco_status_string", "loco_last_error")
 
 
 class LocoError(RuntimeError):
@@ -71,6 +71,11 @@ lib.loco_decode_reduce.restype = ctypes.c_int
 lib.loco_adam_step.argtypes = [ctypes.POINTER(loco_config), _vp, _vp, _i32, _i64, _vp, _vp, _vp,
                                ctypes.POINTER(loco_adam_hparams), _i64, _vp]
 lib.loco_adam_step.restype = ctypes.c_int
+lib.loco_adam_step_bf16.argtypes = [ctypes.POINTER(loco_config), _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
+                                    ctypes.POINTER(loco_adam_hparams), _i64, _vp]
+lib.loco_adam_step_bf16.restype = ctypes.c_int
+lib.loco_sgd_step.argtypes = [ctypes.POINTER(loco_config), _vp, _vp, _i32, _i64, _vp, _vp, ctypes.c_float, _vp]
+lib.loco_sgd_step.restype = ctypes.c_int
 lib.loco_status_string.argtypes = [ctypes.c_int]
 lib.loco_status_string.restype = ctypes.c_char_p
 lib.loco_last_error.argtypes = []
@@ -164,3 +169,18 @@ def loco_adam_step(cfg: loco_config, codes, scales, n: int, param, m, v, hp: loc
     W, ca, sa = _rank_arrays(codes, scales)
     _check(lib.loco_adam_step(ctypes.byref(cfg), ca, sa, W, n, _addr(param), _addr(m), _addr(v),
                               ctypes.byref(hp), t, _stream(stream)))
+
+
+def loco_adam_step_bf16(cfg: loco_config, codes, scales, n: int, param, m, v, param_bf16, hp: loco_adam_hparams,
+                        t: int, *, stream=None):
+    """loco_adam_step that also writes bf16(param) into param_bf16."""
+    W, ca, sa = _rank_arrays(codes, scales)
+    _check(lib.loco_adam_step_bf16(ctypes.byref(cfg), ca, sa, W, n, _addr(param), _addr(m), _addr(v),
+                                   _addr(param_bf16), ctypes.byref(hp), t, _stream(stream)))
+
+
+def loco_sgd_step(cfg: loco_config, codes, scales, n: int, param, lr: float, *, param_bf16=None, stream=None):
+    """Decode-reduce fused with one LoCo-SGD step (param -= lr * mean), optional bf16 copy."""
+    W, ca, sa = _rank_arrays(codes, scales)
+    _check(lib.loco_sgd_step(ctypes.byref(cfg), ca, sa, W, n, _addr(param), _addr(param_bf16), float(lr),
+                             _stream(stream)))

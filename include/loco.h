@@ -186,6 +186,30 @@ loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes,
                            float* param, float* m, float* v,
                            const loco_adam_hparams* hp, int64_t t, loco_stream_t stream);
 
+/*
+ * loco_adam_step_bf16 — loco_adam_step that also writes the updated parameters
+ * rounded to bf16 (nearest, halves to even) into param_bf16 [n] (device,
+ * 16-byte aligned, out): the 16-bit parameter copy a sharded data-parallel job
+ * all-gathers after the update (the 16-bit parameters of the Table I memory
+ * and communication comparison, §4).  Everything else as loco_adam_step.
+ */
+loco_status loco_adam_step_bf16(const loco_config* cfg, const uint8_t* const* codes,
+                                const float* const* scales, int32_t W, int64_t n,
+                                float* param, float* m, float* v, uint16_t* param_bf16,
+                                const loco_adam_hparams* hp, int64_t t, loco_stream_t stream);
+
+/*
+ * loco_sgd_step — loco_decode_reduce fused with one LoCo-SGD step (§4: the
+ * SGD iterate theta_{k+1} = theta_k - eta * g~_k with g~ from Eqn 8):
+ *   p = p - lr*g~          (one fp32 product, one fp32 subtraction)
+ * g~ is formed exactly as in loco_decode_reduce and never written to memory.
+ * param [n] device fp32, in/out.  param_bf16 [n] device, out, or NULL: when
+ * given it receives the updated parameters rounded to bf16 (nearest even).
+ */
+loco_status loco_sgd_step(const loco_config* cfg, const uint8_t* const* codes,
+                          const float* const* scales, int32_t W, int64_t n,
+                          float* param, uint16_t* param_bf16, float lr, loco_stream_t stream);
+
 /* Static text for a status code. */
 const char* loco_status_string(loco_status s);
 

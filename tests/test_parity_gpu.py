@@ -350,3 +350,52 @@ def test_compress_tiny_blocks(L, bits):
         assert_bits_equal(s8.cpu().numpy(), os8, "e8 scales")
         assert_bits_equal(qe.cpu().numpy(), qe_h, "e8 err codes")
         assert_bits_equal(de.cpu().numpy(), de_h, "e8 err steps")
+
+
+@pytest.mark.parametrize("W", [1, 3, 8, 16])
+@pytest.mark.parametrize("bits,block", [(4, 256), (8, 64), (4, 128)])
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_sgd_parity(L, W, bits, block, bf16_out):
+    cfg = L.make_config(bits=bits, block=block)
+    for i, n in enumerate([7, 1000, (1 << 16) + 5, 3 * 4096 + 17]):
+        p = wl().fill_uniform(torch.empty(n, device=DEV), 40 + i, -0.05, 0.05)
+        ph = p.cpu().numpy().copy()
+        pb = Guarded(2 * n, torch.int16) if bf16_out else None
+        pb_h = np.zeros(n, dtype=np.uint16) if bf16_out else None
+        for t in (1, 2, 3):
+            codes, scales = _random_ranks(L, n, bits, block, W, 11 * t + i)
+            L.loco_sgd_step(cfg, codes, scales, n, p, 3e-3, param_bf16=pb.view() if bf16_out else None)
+            oracle.sgd_step([c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales], n, ph,
+                            bits=bits, block=block, lr=3e-3, param_bf16=pb_h)
+            torch.cuda.synchronize()
+            assert_bits_equal(p.cpu().numpy(), ph, f"sgd param n={n} t={t}")
+            if bf16_out:
+                assert_bits_equal(pb.view().cpu().numpy().view(np.uint16), pb_h, f"sgd bf16 n={n} t={t}")
+                assert pb.intact()
+
+
+@pytest.mark.parametrize("W", [1, 8, 13])
+@pytest.mark.parametrize("bits,block", [(4, 256), (8, 128)])
+def test_adam_bf16_parity(L, W, bits, block):
+    cfg = L.make_config(bits=bits, block=block)
+    hpk = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, bias_correction=True,
+               eps_inside_sqrt=False)
+    hp = L.make_adam(**hpk)
+    for i, n in enumerate([9, 5000, (1 << 16) + 3]):
+        p = wl().fill_uniform(torch.empty(n, device=DEV), 60 + i, -0.05, 0.05)
+        m = torch.zeros(n, device=DEV)
+        v = torch.zeros(n, device=DEV)
+        pb = Guarded(2 * n, torch.int16)
+        ph, mh, vh = p.cpu().numpy().copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+        pb_h = np.zeros(n, dtype=np.uint16)
+        for t in (1, 2):
+            codes, scales = _random_ranks(L, n, bits, block, W, 5 * t + i)
+            L.loco_adam_step_bf16(cfg, codes, scales, n, p, m, v, pb.view(), hp, t)
+            oracle.adam_step([c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales], n, ph, mh, vh,
+                             t, bits=bits, block=block, param_bf16=pb_h, **hpk)
+            torch.cuda.synchronize()
+            assert_bits_equal(p.cpu().numpy(), ph, f"param n={n} t={t}")
+            assert_bits_equal(m.cpu().numpy(), mh, f"m n={n} t={t}")
+            assert_bits_equal(v.cpu().numpy(), vh, f"v n={n} t={t}")
+            assert_bits_equal(pb.view().cpu().numpy().view(np.uint16), pb_h, f"bf16 n={n} t={t}")
+            assert pb.intact()

@@ -256,3 +256,26 @@ def test_llama2_7b_fullsize_e8(L):
         assert_bits_equal(scale_rows(scales, s.ids), os_, f"e8 scales step {k}")
         assert_bits_equal(s.grab(qe).numpy(), qe_h, f"e8 err codes step {k}")
         assert_bits_equal(scale_rows(de, s.ids), de_h, f"e8 err steps step {k}")
+
+
+def test_sweep_max_size_sgd_bf16(L):
+    """LoCo-SGD with the bf16 parameter copy at 2^31 + 37 elements (W = 4, 8-bit, block 128)."""
+    n, W, bits, block = (1 << 31) + 37, 4, 8, 128
+    cfg = L.make_config(bits=bits, block=block)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(77)
+    codes = [torch.randint(0, 256, (cb,), dtype=torch.uint8, device=DEV, generator=gen) for _ in range(W)]
+    scales = [torch.rand(nb, device=DEV, generator=gen) * 1e-3 for _ in range(W)]
+    p = W_().fill_uniform(torch.empty(n, device=DEV), 2, -0.02, 0.02)
+    pb = torch.empty(n, dtype=torch.int16, device=DEV)
+    s = Sampler(n, block, 12)
+    ph = s.grab(p).numpy().copy()
+    L.loco_sgd_step(cfg, codes, scales, n, p, 1e-2, param_bf16=pb)
+    rows = [code_rows(c, s.ids, block, bits) for c in codes]
+    srows = [scale_rows(x, s.ids) for x in scales]
+    pb_h = np.zeros(s.idx.numel(), dtype=np.uint16)
+    oracle.sgd_step(rows, srows, s.idx.numel(), ph, bits=bits, block=block, lr=1e-2, param_bf16=pb_h)
+    torch.cuda.synchronize()
+    assert_bits_equal(s.grab(p).numpy(), ph, "sgd param")
+    assert_bits_equal(s.grab(pb).numpy().view(np.uint16), pb_h, "sgd bf16")
