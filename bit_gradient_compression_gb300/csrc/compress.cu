@@ -32,7 +32,6 @@ __device__ __forceinline__ void compress8(const CompressArgs& a, int64_t e0, int
   constexpr int G = BLOCK / 8;  // lanes per quant block
   constexpr float QMAX = float((1 << (BITS - 1)) - 1);
   constexpr float QMIN = -float(1 << (BITS - 1));
-  constexpr uint32_t FIELD = (1u << BITS) - 1u;
 
   // Eqn (2): compensate; block absmax.
   float h[8];
@@ -67,9 +66,9 @@ __device__ __forceinline__ void compress8(const CompressArgs& a, int64_t e0, int
   float inv_e = __fmul_rn(a.kappa, inv);  // s_e = kappa * s; code 0 if it overflows
   if (isinf(inv_e)) inv_e = 0.0f;
 
-  // Eqns (1),(3),(4),(5),(7) per element.
-  uint32_t packed[BITS == 4 ? 1 : 2] = {};
-  uint32_t epacked[2] = {};
+  // Eqns (1),(3),(4),(5),(7) per element.  tq / teq hold the float whose low
+  // byte is the two's-complement code (1.5*2^23 + q).
+  uint32_t tq[8], teq[8];
   float en[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -79,26 +78,46 @@ __device__ __forceinline__ void compress8(const CompressArgs& a, int64_t e0, int
     // which rounds to at most qmax; only a fixed scale can push x past the range.
     if constexpr (FIXED) x = fminf(fmaxf(x, QMIN), QMAX);
     const float t = __fadd_rn(x, kRoundMagic);  // rint, halves to even
-    const uint32_t code = __float_as_uint(t) & FIELD;
-    if constexpr (BITS == 4)
-      packed[0] |= code << (4 * j);
-    else
-      packed[j >> 2] |= code << (8 * (j & 3));
+    tq[j] = __float_as_uint(t);
     const float q = __fsub_rn(t, kRoundMagic);
     const float d = __fmul_rn(q, delta);
     const float r = __fsub_rn(h[j], d);
     float v = __fadd_rn(__fmul_rn(a.beta, e[j]), __fmul_rn(a.one_minus_beta, r));
     if constexpr (E8) {
-      // Eqn (7): e = Round_8-bit(s_e * e~), zero on a reset step.
+      // Eqn (7): e = Round_8-bit(s_e * e~).
       float xe = __fmul_rn(v, inv_e);
       xe = fminf(fmaxf(xe, -128.0f), 127.0f);
-      const uint32_t qe = a.reset ? 0u : (__float_as_uint(__fadd_rn(xe, kRoundMagic)) & 0xFFu);
-      epacked[j >> 2] |= qe << (8 * (j & 3));
+      teq[j] = __float_as_uint(__fadd_rn(xe, kRoundMagic));
     } else {
       v = (v < elo) ? elo : v;
       v = (v > ehi) ? ehi : v;
-      en[j] = a.reset ? 0.0f : v;
+      en[j] = v;
     }
+  }
+  // Reset step of Eqn (7): the stored error becomes 0 (a uniform branch).
+  if (a.reset) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      en[j] = 0.0f;
+      teq[j] = 0u;
+    }
+  }
+  // Pack the low bytes / nibbles with byte permutes.
+  uint32_t packed[BITS == 4 ? 1 : 2];
+  if constexpr (BITS == 8) {
+    packed[0] = __byte_perm(__byte_perm(tq[0], tq[1], 0x0040), __byte_perm(tq[2], tq[3], 0x0040), 0x5410);
+    packed[1] = __byte_perm(__byte_perm(tq[4], tq[5], 0x0040), __byte_perm(tq[6], tq[7], 0x0040), 0x5410);
+  } else {
+    // byte k = (code_{2k} & 0xF) | (code_{2k+1} << 4)
+    uint32_t b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) b[k] = (tq[2 * k] & 0xFu) | ((tq[2 * k + 1] << 4) & 0xF0u);
+    packed[0] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+  }
+  uint32_t epacked[2] = {0u, 0u};
+  if constexpr (E8) {
+    epacked[0] = __byte_perm(__byte_perm(teq[0], teq[1], 0x0040), __byte_perm(teq[2], teq[3], 0x0040), 0x5410);
+    epacked[1] = __byte_perm(__byte_perm(teq[4], teq[5], 0x0040), __byte_perm(teq[6], teq[7], 0x0040), 0x5410);
   }
 
   // Stores: codes and the block step inside the padded code range, the error
