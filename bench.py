@@ -287,6 +287,24 @@ def cpu_baseline(w, S, steps, warmup):
             "ms_per_step": dt * 1e3}
 
 
+# ----------------------------------------------------------------------------- multi-rank
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over all ranks (a no-op on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_value(units_per_rank_step: int, world: int, ms_per_step_max: float) -> float:
+    """Units every rank processed in one step, over the slowest rank's step time (GB/s)."""
+    return world * units_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, param, m, v, world, dist, h2d, d2h):
@@ -489,13 +507,9 @@ def run_loco(args, rank, world):
                       h2d, d2h)
 
     units_step = sum(grad_units(n, gsize, W).values())
-    t_ms = total_ms / args.steps
-    if world > 1:
-        tt = torch.tensor([t_ms, e2e[0] if e2e else 0.0], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms, e2e_max = float(tt[0]), float(tt[1])
-        if e2e:
-            e2e = (e2e_max, e2e[1], e2e[2])
+    t_ms, e2e_max = max_over_ranks([total_ms / args.steps, e2e[0] if e2e else 0.0], dev)
+    if e2e:
+        e2e = (e2e_max, e2e[1], e2e[2])
     if rank != 0:
         return None
 
@@ -511,7 +525,7 @@ def run_loco(args, rank, world):
                    "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured" else
                    "fallback"}
     dominant = max(per_kernel, key=per_kernel.get)
-    value = world * units_step / (t_ms * 1e-3) / 1e9
+    value = whole_job_value(units_step, world, t_ms)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -532,7 +546,7 @@ def run_loco(args, rank, world):
                       "skipped": e2e_skip}
     if e2e:
         e2e_ms, h2d, d2h = e2e
-        out["e2e"] = {"value": round(world * units_step / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+        out["e2e"] = {"value": round(whole_job_value(units_step, world, e2e_ms), 1), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                       "steps": args.e2e_steps,
                       "what": "page-locked host -> device: rank 0 gradient + ranks 1..W-1 packed buffers; "
