@@ -57,6 +57,11 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--error-storage", default="fp32", choices=["fp32", "int8"],
                     help="compensation error kept in fp32 (default) or as int8 codes + per-block step")
+    ap.add_argument("--optimizer", default="adam", choices=["adam", "sgd"],
+                    help="optimizer fused with the receiver average (default adam)")
+    ap.add_argument("--param-bf16", action="store_true", help="also write the bf16 copy of the updated parameters")
+    ap.add_argument("--fixed-scale", type=float, default=None,
+                    help="paper-literal fixed quantisation scale s (e.g. 524288 = 2^19) instead of blockwise absmax")
     return ap.parse_args()
 
 
@@ -77,19 +82,20 @@ def workload(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
-def kernel_bytes(n, gsize, bits, block, W, e8=False):
+def kernel_bytes(n, gsize, bits, block, W, e8=False, optimizer="adam", bf16_out=False):
     nb = -(-n // block)
     cb = nb * block * bits // 8
     sb = nb * 4
+    opt_state = 24 if optimizer == "adam" else 8   # param (+ m, v) read and written
     return {
         "compress": n * gsize + (2 * n + 3 * sb if e8 else 8 * n) + cb + sb,
         "decode_reduce": W * (cb + sb) + 4 * n,
-        "adam": W * (cb + sb) + 24 * n,
+        optimizer: W * (cb + sb) + opt_state * n + (2 * n if bf16_out else 0),
     }
 
 
-def grad_units(n, gsize, W):
-    return {"compress": n * gsize, "decode_reduce": W * n * gsize, "adam": W * n * gsize}
+def grad_units(n, gsize, W, optimizer="adam"):
+    return {"compress": n * gsize, "decode_reduce": W * n * gsize, optimizer: W * n * gsize}
 
 
 def peaks():
@@ -258,32 +264,37 @@ def oracle_sample(w, S, seed=7):
     return g0, e, codes, scales, p, np.zeros(S, np.float32), np.zeros(S, np.float32)
 
 
-def oracle_step(w, S, inp, step, threads):
+def oracle_step(w, S, inp, step, threads, optimizer="adam"):
     import oracle
     g0, e, codes, scales, p, m, v = inp
     c0, s0 = oracle.compress(g0, e, step, bits=w.bits, block=w.block, beta=0.9, kappa=4.0, reset_period=512,
                              threads=threads)
     allc, alls = [c0] + codes, [s0] + scales
     oracle.decode_reduce(allc, alls, S, bits=w.bits, block=w.block, threads=threads)
-    oracle.adam_step(allc, alls, S, p, m, v, step, bits=w.bits, block=w.block, lr=1e-4, beta1=0.9, beta2=0.95,
-                     eps=1e-8, threads=threads)
+    if optimizer == "sgd":
+        oracle.sgd_step(allc, alls, S, p, bits=w.bits, block=w.block, lr=1e-3, threads=threads)
+    else:
+        oracle.adam_step(allc, alls, S, p, m, v, step, bits=w.bits, block=w.block, lr=1e-4, beta1=0.9, beta2=0.95,
+                         eps=1e-8, threads=threads)
 
 
-def cpu_baseline(w, S, steps, warmup):
-    """Times the oracle, as it stands, on all host cores over an S-element sample."""
+def cpu_baseline(w, S, steps, warmup, optimizer="adam"):
+    """Times the oracle, as it stands, on all host cores over an S-element sample
+    of the step (fp32 error, absmax scale, the given optimizer)."""
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     inp = oracle_sample(w, S)
     gsize = 2 if "bf16" in str(w.grad_dtype) else 4
     for k in range(warmup):
-        oracle_step(w, S, inp, k + 1, threads)
+        oracle_step(w, S, inp, k + 1, threads, optimizer)
     t0 = time.perf_counter()
     for k in range(steps):
-        oracle_step(w, S, inp, warmup + k + 1, threads)
+        oracle_step(w, S, inp, warmup + k + 1, threads, optimizer)
     dt = (time.perf_counter() - t0) / steps
-    units = sum(grad_units(S, gsize, w.W).values())
+    units = sum(grad_units(S, gsize, w.W, optimizer).values())
     return {"value": units / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"first {S:,} elements of the {w.name} bucket (rank 0 compress + decode-reduce + Adam over "
-                      f"W={w.W} ranks), {steps} timed step(s) after {warmup} warm-up, same gradient law on host",
+            "sample": f"first {S:,} elements of the {w.name} bucket (rank 0 compress + decode-reduce + "
+                      f"{'SGD' if optimizer == 'sgd' else 'Adam'} over W={w.W} ranks, fp32 error, absmax scale), "
+                      f"{steps} timed step(s) after {warmup} warm-up, same gradient law on host",
             "ms_per_step": dt * 1e3}
 
 
@@ -307,7 +318,7 @@ def whole_job_value(units_per_rank_step: int, world: int, ms_per_step_max: float
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, param, m, v, world, dist, h2d, d2h):
+def run_e2e(args, L, w, cfg, n, nb, cb, g, compress, update, codes, scales, mean, world, dist, h2d, d2h):
     """The step through the public API with its inputs coming from page-locked
     host memory and its output (rank 0's packed buffer, the bytes a rank sends)
     going back to it, every step, inside the timed region.
@@ -342,6 +353,23 @@ def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, pa
     sets = [(g, codes, scales),
             (torch.empty_like(g), [torch.empty_like(c) for c in codes], [torch.empty_like(x) for x in scales])]
     torch.cuda.synchronize()
+    # This machine's host link, measured on the same page-locked buffer just before
+    # the timed region (it varies between boxes), reported beside the e2e number.
+    probe_n = min(g_h.numel() * g_h.element_size(), 4 << 30)
+    src = g_h.view(torch.uint8)[:probe_n]
+    dst = g.view(torch.uint8)[:probe_n]
+    link = []
+    for dst_, src_ in ((dst, src), (src, dst)):
+        dst_.copy_(src_, non_blocking=True)
+        torch.cuda.synchronize()
+        a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(comp)
+        dst_.copy_(src_, non_blocking=True)
+        b0.record(comp)
+        torch.cuda.synchronize()
+        link.append(probe_n / (a0.elapsed_time(b0) * 1e-3) / 1e9)
+    g.copy_(g_h)
+    torch.cuda.synchronize()
     K = args.e2e_steps
     ev = lambda: torch.cuda.Event()
     g_done, in_done, comp_done, c0_done, out_done = [[ev() for _ in range(K)] for _ in range(5)]
@@ -370,7 +398,7 @@ def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, pa
         c0_done[k].record(comp)
         comp.wait_event(in_done[k])            # ranks 1..W-1 arrived
         L.loco_decode_reduce(cfg, ck, sk, n, mean, stream=comp)
-        L.loco_adam_step(cfg, ck, sk, n, param, m, v, hp, k + 1, stream=comp)
+        update(ck, sk, k + 1, stream=comp)
         comp_done[k].record(comp)
         with torch.cuda.stream(s_out):         # output of step k
             s_out.wait_event(c0_done[k])
@@ -385,7 +413,7 @@ def run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, pa
     for h in hosts:
         torch.cuda.cudart().cudaHostUnregister(h.data_ptr())
     del sets[1]
-    return (ms, h2d, d2h)
+    return (ms, h2d, d2h, link)
 
 
 def run_loco(args, rank, world):
@@ -403,7 +431,9 @@ def run_loco(args, rank, world):
     gsize = 2 if w.grad_dtype == torch.bfloat16 else 4
     # beta weights the previous error; the 8-bit storage needs weight on the new error (see loco.h)
     cfg = L.make_config(bits=bits, block=block, beta=0.9 if args.error_storage == "fp32" else 0.1,
-                        err_scale_mult=4.0, reset_period=512)
+                        err_scale_mult=4.0, reset_period=512, fixed_scale=args.fixed_scale)
+    opt = args.optimizer
+    pb16 = torch.empty(n, dtype=torch.int16, device=dev) if args.param_bf16 else None
     hp = L.make_adam(lr=1e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)
     nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
 
@@ -437,9 +467,17 @@ def run_loco(args, rank, world):
     zero_error()
     mean = torch.empty(n, dtype=torch.float32, device=dev)
     param = wl.fill_uniform(torch.empty(n, device=dev), 3, -0.02, 0.02)
-    m = torch.zeros(n, device=dev)
-    v = torch.zeros(n, device=dev)
+    m = torch.zeros(n, device=dev) if opt == "adam" else None
+    v = torch.zeros(n, device=dev) if opt == "adam" else None
     torch.cuda.synchronize()
+
+    def update(ck, sk, k, stream=None):
+        if opt == "sgd":
+            L.loco_sgd_step(cfg, ck, sk, n, param, 1e-3, param_bf16=pb16, stream=stream)
+        elif pb16 is not None:
+            L.loco_adam_step_bf16(cfg, ck, sk, n, param, m, v, pb16, hp, k, stream=stream)
+        else:
+            L.loco_adam_step(cfg, ck, sk, n, param, m, v, hp, k, stream=stream)
 
     stream = torch.cuda.current_stream()
     step_no = [0]
@@ -455,7 +493,7 @@ def run_loco(args, rank, world):
         L.loco_decode_reduce(cfg, codes, scales, n, mean)
         if ev:
             ev[2].record(stream)
-        L.loco_adam_step(cfg, codes, scales, n, param, m, v, hp, k)
+        update(codes, scales, k)
         if ev:
             ev[3].record(stream)
 
@@ -484,7 +522,7 @@ def run_loco(args, rank, world):
     per_kernel = {
         "compress": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
         "decode_reduce": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
-        "adam": statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs),
+        opt: statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs),
     }
 
     # ---- e2e: host buffers in page-locked memory, copies inside the timed region
@@ -503,25 +541,26 @@ def run_loco(args, rank, world):
         if h2d + d2h > 0.9 * free_dev:
             e2e_skip = f"second device buffer set needs {(h2d + d2h) / 1e9:.1f} GB, {free_dev / 1e9:.1f} GB free"
     if e2e_skip is None:
-        e2e = run_e2e(args, L, w, cfg, hp, n, nb, cb, g, compress, codes, scales, mean, param, m, v, world, dist,
-                      h2d, d2h)
+        e2e = run_e2e(args, L, w, cfg, n, nb, cb, g, compress, update, codes, scales, mean, world, dist, h2d, d2h)
 
-    units_step = sum(grad_units(n, gsize, W).values())
+    units_step = sum(grad_units(n, gsize, W, opt).values())
     t_ms, e2e_max = max_over_ranks([total_ms / args.steps, e2e[0] if e2e else 0.0], dev)
     if e2e:
-        e2e = (e2e_max, e2e[1], e2e[2])
+        e2e = (e2e_max,) + tuple(e2e[1:])
     if rank != 0:
         return None
 
     hbm, hbm_kind = peaks()
-    kb = kernel_bytes(n, gsize, bits, block, W, e8)
+    default_step = not e8 and opt == "adam" and pb16 is None and args.fixed_scale is None
+    kb = kernel_bytes(n, gsize, bits, block, W, e8, opt, pb16 is not None)
     roof = {}
     for k, ms in per_kernel.items():
         ach = kb[k] / (ms * 1e-3) / 1e9
         roof[k] = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                    "frac": round(ach / hbm, 4), "ms": round(ms, 4),
-                   "traffic": ncu_traffic(k, kb[k], n, w.name) if not e8 else None, "algorithmic_bytes": kb[k],
-                   "grad_GBps": round(grad_units(n, gsize, W)[k] / (ms * 1e-3) / 1e9, 1),
+                   "traffic": ncu_traffic(k, kb[k], n, w.name) if default_step else None,
+                   "algorithmic_bytes": kb[k],
+                   "grad_GBps": round(grad_units(n, gsize, W, opt)[k] / (ms * 1e-3) / 1e9, 1),
                    "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured" else
                    "fallback"}
     dominant = max(per_kernel, key=per_kernel.get)
@@ -532,8 +571,11 @@ def run_loco(args, rank, world):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "n_elements": n, "grad_dtype": "bf16" if gsize == 2 else "fp32",
                    "bits": bits, "block": block, "W": W, "beta": cfg.beta, "kappa": 4.0,
-                   "error_storage": args.error_storage,
-                   "step": ("loco_compress_e8" if e8 else "loco_compress") + "(rank 0) + loco_decode_reduce(W) + loco_adam_step(W)",
+                   "error_storage": args.error_storage, "optimizer": opt,
+                   "step": ("loco_compress_e8" if e8 else "loco_compress") + "(rank 0) + loco_decode_reduce(W) + "
+                           + {"adam": "loco_adam_step" + ("_bf16" if pb16 is not None else ""),
+                              "sgd": "loco_sgd_step" + (" (bf16 copy)" if pb16 is not None else "")}[opt] + "(W)",
+                   "scale": "absmax" if args.fixed_scale is None else f"fixed s={args.fixed_scale:g}",
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU, W ranks simulated in HBM"},
         "roofline": dict(roof[dominant], kernel=dominant),
@@ -545,10 +587,12 @@ def run_loco(args, rank, world):
         out["e2e"] = {"value": None, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "skipped": e2e_skip}
     if e2e:
-        e2e_ms, h2d, d2h = e2e
+        e2e_ms, h2d, d2h, link = e2e
         out["e2e"] = {"value": round(whole_job_value(units_step, world, e2e_ms), 1), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                       "steps": args.e2e_steps,
+                      "host_link_GBps": {"h2d": round(link[0], 1), "d2h": round(link[1], 1)},
+                      "copy_bound_ms_per_step": round(h2d / (link[0] * 1e9) * 1e3, 1),
                       "what": "page-locked host -> device: rank 0 gradient + ranks 1..W-1 packed buffers; "
                               "device -> page-locked host: rank 0's packed buffer; copies on their own streams "
                               "overlap the previous step's kernels (double-buffered device inputs)"}
@@ -585,7 +629,7 @@ def main():
         w = workload(args.workload)
         S = min(w.n, 1 << 27)
         try:
-            out["cpu_baseline"] = cpu_baseline(w, S, 1, 1)
+            out["cpu_baseline"] = cpu_baseline(w, S, 1, 1, args.optimizer)
         except Exception as ex:  # the GPU numbers stand without it
             out["cpu_baseline"] = {"value": None, "error": repr(ex)}
         print(json.dumps(out), flush=True)
