@@ -24,7 +24,9 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "loco_oracle.c")
-_LIB = os.path.join(_HERE, "libloco_oracle.so")
+# A test may point the oracle at another build of this source (the mutation
+# test does, to check that the pins catch planted mistakes).
+_LIB = os.environ.get("LOCO_ORACLE_LIB") or os.path.join(_HERE, "libloco_oracle.so")
 
 # -ffp-contract=off: every product and sum is its own rounded fp32 operation.
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
@@ -35,6 +37,8 @@ _lock = threading.Lock()
 
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/libloco_oracle.so`` (gcc)."""
+    if os.environ.get("LOCO_ORACLE_LIB"):
+        return _LIB
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])

@@ -1,0 +1,85 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/loco_oracle.c (a dropped
+term, a swapped weight, a wrong sign or index, the wrong rounding rule, ...),
+builds it, and runs the CPU pin tests against it in a subprocess: at least one
+pin must fail.  The unmodified source must pass the same tests.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "loco_oracle.c")
+PIN_TESTS = ["tests/test_oracle_golden.py", "tests/test_oracle_pins.py", "tests/test_oracle_e8.py"]
+
+# (name, text in the source, replacement, occurrence to replace (0 = all))
+MUTATIONS = [
+    ("round half away from zero", "return (int)nearbyintf(x);", "return (int)roundf(x);", 0),
+    ("compensation term dropped", "h[j] = g + err[lo + j];", "h[j] = g;", 0),
+    ("beta weights swapped", "float t1 = beta * prev;", "float t1 = one_minus_beta * prev;", 1),
+    ("residual sign flipped", "float r = h[j] - d;", "float r = d - h[j];", 1),
+    ("nibble order swapped", "if (j % 2 == 0)\n      blk[j / 2] = (uint8_t)((blk[j / 2] & 0xF0) | nib);",
+     "if (j % 2 == 1)\n      blk[j / 2] = (uint8_t)((blk[j / 2] & 0xF0) | nib);", 0),
+    ("clip bound off by one code", "const float e_lo = -128.0f * delta_e;", "const float e_lo = -127.0f * delta_e;", 0),
+    ("reset one step late", "(step % reset_period == 0)", "((step - 1) % reset_period == 0)", 1),
+    ("scale uses qmax+1", "delta = amax / qmax;", "delta = amax / (qmax + 1.0f);", 1),
+    ("last rank dropped from the mean", "for (int w = 0; w < W; ++w) {\n      int q = get_code(codes[w] + b * bytes_per_block, bits, j);\n      float d = (float)q * scales[w][b];\n      acc = (w == 0) ? d : acc + d;\n      acc64 += (double)d;",
+     "for (int w = 0; w < W - (W > 1); ++w) {\n      int q = get_code(codes[w] + b * bytes_per_block, bits, j);\n      float d = (float)q * scales[w][b];\n      acc = (w == 0) ? d : acc + d;\n      acc64 += (double)d;", 0),
+    ("Adam first moment weights swapped", "float mi = beta1 * m[i];\n    float mg = omb1 * g;",
+     "float mi = omb1 * m[i];\n    float mg = beta1 * g;", 0),
+    ("Adam bias correction of v dropped", "c2 = eps_inside_sqrt ? (float)(1.0 / bc2) : (float)(1.0 / sqrt(bc2));",
+     "c2 = 1.0f;", 0),
+    ("8-bit error scale divides by kappa", "float inv_e = kappa * inv;", "float inv_e = inv / kappa;", 0),
+    ("8-bit error not decompressed", "prev[j] = (float)err_codes[lo + j] * de_prev;", "prev[j] = (float)err_codes[lo + j];", 0),
+    ("bf16 truncation instead of rounding", "u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;", 0),
+    ("SGD step sign flipped", "float p = param[i] - step;", "float p = param[i] + step;", 0),
+]
+
+
+def _build(src_text, out_dir, name):
+    import oracle
+    c = os.path.join(out_dir, f"{name}.c")
+    so = os.path.join(out_dir, f"lib{name}.so")
+    with open(c, "w") as f:
+        f.write(src_text)
+    subprocess.check_call(["gcc", *oracle.CFLAGS, c, "-o", so, "-lm"])
+    return so
+
+
+def _run_pins(so):
+    env = dict(os.environ, LOCO_ORACLE_LIB=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "not gpu", "-p", "no:cacheprovider",
+                        *PIN_TESTS], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode, r.stdout[-2000:]
+
+
+def _mutate(text, old, new, occurrence):
+    assert old in text, f"mutation anchor not found: {old[:60]!r}"
+    if occurrence == 0:
+        return text.replace(old, new)
+    idx = -1
+    for _ in range(occurrence):
+        idx = text.index(old, idx + 1)
+    return text[:idx] + new + text[idx + len(old):]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+def test_unmodified_oracle_passes(source, tmp_path):
+    so = _build(source, str(tmp_path), "loco_oracle_copy")
+    rc, out = _run_pins(so)
+    assert rc == 0, out
+
+
+@pytest.mark.parametrize("name,old,new,occurrence", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(source, tmp_path, name, old, new, occurrence):
+    so = _build(_mutate(source, old, new, occurrence), str(tmp_path), "loco_oracle_mut")
+    rc, out = _run_pins(so)
+    assert rc != 0, f"no pin caught the planted mistake: {name}\n{out}"
