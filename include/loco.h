@@ -25,6 +25,12 @@
  *    8-bit codes are int8.  Padding elements of a ragged last block get code 0.
  *  - Alignment: grad, err, codes, mean, param, m, v must be 16-byte aligned;
  *    scales 4-byte aligned (LOCO_ERR_MISALIGNED otherwise).
+ *  - The calls allocate nothing and never synchronise, so they can be captured
+ *    in a CUDA graph.  Step counters, the reset decision and the Adam constants
+ *    are computed on the host at call time and become part of the captured
+ *    launch: a graph captured at step k replays step k.  The first call of each
+ *    configuration (bits, block, W, dtype, ...) queries occupancy and sets the
+ *    kernel's shared-memory limit once; make it before capturing.
  *  - Arithmetic is IEEE binary32, round to nearest even, no fused
  *    multiply-add; the exact operation order of each step is stated at the
  *    entry point.  Non-finite inputs are outside the contract: no call reads

@@ -399,3 +399,51 @@ def test_adam_bf16_parity(L, W, bits, block):
             assert_bits_equal(v.cpu().numpy(), vh, f"v n={n} t={t}")
             assert_bits_equal(pb.view().cpu().numpy().view(np.uint16), pb_h, f"bf16 n={n} t={t}")
             assert pb.intact()
+
+
+def test_cuda_graph_capture_replays_the_step(L):
+    """The entry points allocate and synchronise nothing, so a whole step
+    (compress W ranks, decode-reduce, Adam) can be captured in a CUDA graph and
+    replayed; the replay gives the same bits as direct calls."""
+    n, bits, block, W = 3 * 4096 + 77, 4, 128, 3
+    cfg = L.make_config(bits=bits, block=block, beta=0.9, reset_period=0)
+    hp = L.make_adam(lr=1e-3, weight_decay=0.01)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+
+    def state():
+        gs = [_grad(n, torch.bfloat16, 200 + w) for w in range(W)]
+        es = [torch.zeros(n, device=DEV) for _ in range(W)]
+        cs = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)]
+        ss = [torch.empty(nb, device=DEV) for _ in range(W)]
+        p = wl().fill_uniform(torch.empty(n, device=DEV), 9, -0.1, 0.1)
+        return gs, es, cs, ss, p, torch.zeros(n, device=DEV), torch.zeros(n, device=DEV), torch.empty(n, device=DEV)
+
+    def step(st, k, stream=None):
+        gs, es, cs, ss, p, m, v, mean = st
+        for w in range(W):
+            L.loco_compress(cfg, gs[w], es[w], k, cs[w], ss[w], stream=stream)
+        L.loco_decode_reduce(cfg, cs, ss, n, mean, stream=stream)
+        L.loco_adam_step(cfg, cs, ss, n, p, m, v, hp, k, stream=stream)
+
+    direct = state()
+    for k in (1, 2, 3):
+        step(direct, k)
+    graphed = state()
+    step(graphed, 1)                         # first call per kernel does its one-time set-up
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        step(graphed, 2, stream=s)
+    g2.replay()
+    g3 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g3, stream=s):
+        step(graphed, 3, stream=s)
+    g3.replay()
+    torch.cuda.synchronize()
+    for a, b, name in zip(direct, graphed, ("g", "e", "codes", "scales", "p", "m", "v", "mean")):
+        if isinstance(a, list):
+            for x, y in zip(a, b):
+                assert torch.equal(x, y), name
+        else:
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
