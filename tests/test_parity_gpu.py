@@ -447,3 +447,44 @@ def test_cuda_graph_capture_replays_the_step(L):
                 assert torch.equal(x, y), name
         else:
             assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
+
+
+@pytest.mark.parametrize("storage", ["fp32", "int8"])
+def test_checkpoint_resume(L, storage):
+    """The sender's whole state is its error buffer(s) and the step counter: a
+    host copy taken after step 3 and restored into fresh buffers continues
+    exactly like the uninterrupted run (reset period 4 fires inside the resumed
+    part)."""
+    n, bits, block = 50_001, 4, 128
+    cfg = L.make_config(bits=bits, block=block, beta=0.3, reset_period=4)
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    grads = [_grad(n, torch.bfloat16, 900 + k) for k in range(1, 8)]
+
+    def new_state():
+        if storage == "fp32":
+            return [torch.zeros(n, device=DEV)]
+        return [torch.zeros(n, dtype=torch.int8, device=DEV), torch.zeros(nb, device=DEV)]
+
+    def run(state, k, c, s):
+        if storage == "fp32":
+            L.loco_compress(cfg, grads[k - 1], state[0], k, c, s)
+        else:
+            L.loco_compress_e8(cfg, grads[k - 1], state[0], state[1], k, c, s)
+
+    full, outs = new_state(), []
+    for k in range(1, 8):
+        c, s = torch.empty(cb, dtype=torch.uint8, device=DEV), torch.empty(nb, device=DEV)
+        run(full, k, c, s)
+        outs.append((c, s))
+    part = new_state()
+    for k in range(1, 4):
+        run(part, k, torch.empty(cb, dtype=torch.uint8, device=DEV), torch.empty(nb, device=DEV))
+    ckpt = [x.cpu().clone() for x in part]            # checkpoint: plain bytes + step = 3
+    del part
+    resumed = [x.to(DEV) for x in ckpt]
+    for k in range(4, 8):
+        c, s = torch.empty(cb, dtype=torch.uint8, device=DEV), torch.empty(nb, device=DEV)
+        run(resumed, k, c, s)
+        assert torch.equal(c, outs[k - 1][0]) and torch.equal(s, outs[k - 1][1]), k
+    for a, b in zip(resumed, full):
+        assert torch.equal(a, b)
