@@ -81,7 +81,7 @@ static int get_code(const uint8_t* blk, int bits, int j) {
  * Sender step of LoCo for the quant blocks [b0, b1) of a bucket of n elements.
  *
  *  §3.1 Eqn (2):  h = g + decompressor(e)           (e stored in fp32 here)
- *  §3.1 Eqns (1),(3): c = Round_p-bit(s*h); this build chooses s per block as
+ *  §3.1 Eqns (1),(3): c = Round_p-bit(s*h); s is chosen per block as
  *                 qmax/A_b (A_b = max|h| of the block), or one fixed s for all
  *                 blocks; the decompressor multiplies the code by Delta = 1/s.
  *  §3.2 Eqn (4),(5): error moving average  e~ = beta*e~_prev + (1-beta)*(h-d)
