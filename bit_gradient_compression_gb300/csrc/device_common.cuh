@@ -61,6 +61,23 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Bulk (TMA) copy shared -> global of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), issued by one thread.  Completion is tracked by
+// bulk groups and waited for with the hardware wait_group instruction.
+__device__ __forceinline__ void fence_smem_to_async_proxy() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The shared-memory source of every committed bulk store has been read.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Multistage tile pipeline.  The CTA walks tiles blockIdx.x, blockIdx.x +
 // gridDim.x, ...; S-1 tiles are in flight (cp.async into their own stage of
@@ -72,9 +89,9 @@ __device__ __forceinline__ void cp_async_wait() {
 //   issue(stage_base, tile): start the copies of one tile (each thread its share)
 //   body(stage_base, tile):  consume one staged tile
 // ---------------------------------------------------------------------------
-template <int S, typename Issue, typename Body>
-__device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, int64_t ntiles, Issue issue,
-                                               Body body) {
+template <int S, typename Issue, typename Body, typename Before, typename After>
+__device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, int64_t ntiles, Issue issue, Body body,
+                                               Before before, After after) {
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) {
     const int64_t tile = blockIdx.x + int64_t(s) * gridDim.x;
@@ -88,12 +105,20 @@ __device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, 
     if (ahead < ntiles) issue(sm + nxt * stage_bytes, ahead);
     cp_async_commit();
     cp_async_wait<S - 1>();
+    before(tile);  // runs before the barrier that publishes the tile
     __syncthreads();
     body(sm + cur * stage_bytes, tile);
     __syncthreads();
+    after(tile);   // runs after every thread has finished the tile
     cur = (cur + 1 == S) ? 0 : cur + 1;
   }
   cp_async_wait<0>();
+}
+
+template <int S, typename Issue, typename Body>
+__device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, int64_t ntiles, Issue issue,
+                                               Body body) {
+  pipeline_tiles<S>(sm, stage_bytes, ntiles, issue, body, [](int64_t) {}, [](int64_t) {});
 }
 
 // ---------------------------------------------------------------------------

@@ -63,11 +63,15 @@ struct Tile {
   }
 };
 
-// Largest stage count <= want whose tiles fit one CTA's shared memory.
+// Largest stage count <= want (at least 1) for which `min_ctas` CTAs, each
+// with S tiles plus `extra` bytes of shared memory, fit on one SM (228 KB,
+// 1 KB reserved per CTA); never more than one CTA's 227 KB limit.
 template <int BITS, int W, int E, int NF>
-constexpr int fit_stages(int want) {
+constexpr int fit_stages(int want, size_t extra = 0, int min_ctas = 1) {
   int s = want;
-  while (s > 1 && size_t(s) * Tile<BITS, W, E, NF>::kBytes > size_t(227) * 1024) --s;
+  while (s > 1 && (size_t(s) * Tile<BITS, W, E, NF>::kBytes + extra > size_t(227) * 1024 ||
+                   size_t(min_ctas) * (size_t(s) * Tile<BITS, W, E, NF>::kBytes + extra + 1024) > size_t(228) * 1024))
+    --s;
   return s;
 }
 
@@ -113,10 +117,11 @@ __device__ __forceinline__ void tile_mean(const Tile<BITS, W, E, NF>& tl, int t,
 }
 
 // Receiver tiles through the multistage pipeline; elements past the last full
-// tile are handled by `tail` in one CTA.
-template <int BITS, int W, int E, int NF, int S, typename Body, typename TailFn>
+// tile are handled by `tail` in one CTA.  `before`/`after` run for thread-level
+// set-up and hand-off around each tile (see pipeline_tiles).
+template <int BITS, int W, int E, int NF, int S, typename Body, typename TailFn, typename Before, typename After>
 __device__ __forceinline__ void tile_pipeline(const float* const* farr, const RankPtrs& rp, int64_t n, int log2_block,
-                                              Body body, TailFn tail) {
+                                              Body body, TailFn tail, Before before, After after) {
   extern __shared__ __align__(16) uint8_t sm[];
   using TL = Tile<BITS, W, E, NF>;
   const int t = threadIdx.x;
@@ -125,13 +130,18 @@ __device__ __forceinline__ void tile_pipeline(const float* const* farr, const Ra
   pipeline_tiles<S>(
       sm, TL::kBytes, ntiles,
       [&](uint8_t* st, int64_t tile) { issue_tile<BITS, W, E, NF>(TL{st}, farr, rp, tile, nsc, t); },
-      [&](uint8_t* st, int64_t tile) { body(TL{st}, tile * TL::T + int64_t(t) * E); });
+      [&](uint8_t* st, int64_t tile) { body(TL{st}, tile * TL::T + int64_t(t) * E); }, before, after);
   if (ntiles * TL::T < n && blockIdx.x == ntiles % gridDim.x) {
     const int64_t e0 = ntiles * TL::T + int64_t(t) * E;
     if (e0 < n) tail(e0);
   }
 }
 
+template <int BITS, int W, int E, int NF, int S, typename Body, typename TailFn>
+__device__ __forceinline__ void tile_pipeline(const float* const* farr, const RankPtrs& rp, int64_t n, int log2_block,
+                                              Body body, TailFn tail) {
+  tile_pipeline<BITS, W, E, NF, S>(farr, rp, n, log2_block, body, tail, [](int64_t) {}, [](int64_t) {});
+}
 
 // bf16 copy of E updated parameters (round to nearest even).
 template <int E>
