@@ -9,6 +9,9 @@ namespace loco {
 #ifndef LOCO_ADAM_ELEMS
 #define LOCO_ADAM_ELEMS(bits) 8
 #endif
+#ifndef LOCO_ADAM_MIN_CTAS
+#define LOCO_ADAM_MIN_CTAS 2  // CTAs per SM the stage count is fitted for (measured best)
+#endif
 #ifndef LOCO_ADAM_STAGES
 #define LOCO_ADAM_STAGES 2
 #endif
@@ -23,8 +26,11 @@ __device__ __forceinline__ void adam_elem(const AdamArgs& a, float g, float& p, 
   p = __fsub_rn(p, __fmul_rn(a.c1, __fdiv_rn(m, den)));
 }
 
+// Three CTAs per SM is what the two-stage staging allows; the bound keeps every
+// rank count within the matching register budget (one instantiation otherwise
+// took 96 registers and ran at two CTAs per SM).
 template <int BITS, int W, int E, int S, bool BF16OUT>
-__global__ void __launch_bounds__(kThreads) k_adam(const AdamArgs a, int log2_block) {
+__global__ void __launch_bounds__(kThreads, 3) k_adam(const AdamArgs a, int log2_block) {
   using TL = Tile<BITS, W, E, 3>;
   const float* farr[3] = {a.param, a.m, a.v};
   tile_pipeline<BITS, W, E, 3, S>(
@@ -71,7 +77,7 @@ struct AdamLaunch {
   struct F {
     static cudaError_t run(const AdamArgs& a, cudaStream_t s) {
       constexpr int E = LOCO_ADAM_ELEMS(BITS);
-      constexpr int S = fit_stages<BITS, W, E, 3>(LOCO_ADAM_STAGES);
+      constexpr int S = fit_stages<BITS, W, E, 3>(LOCO_ADAM_STAGES, 0, LOCO_ADAM_MIN_CTAS);
       constexpr size_t smem = S * Tile<BITS, W, E, 3>::kBytes;
       static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
       const void* fn = reinterpret_cast<const void*>(&k_adam<BITS, W, E, S, BF16OUT>);

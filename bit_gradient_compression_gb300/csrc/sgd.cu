@@ -9,6 +9,9 @@ namespace loco {
 #ifndef LOCO_SGD_ELEMS
 #define LOCO_SGD_ELEMS(bits) (64 / (bits))
 #endif
+#ifndef LOCO_SGD_MIN_CTAS
+#define LOCO_SGD_MIN_CTAS 3  // CTAs per SM the stage count is fitted for (measured best)
+#endif
 #ifndef LOCO_SGD_STAGES
 #define LOCO_SGD_STAGES 3
 #endif
@@ -51,7 +54,7 @@ struct SgdLaunch {
   struct F {
     static cudaError_t run(const SgdArgs& a, cudaStream_t s) {
       constexpr int E = LOCO_SGD_ELEMS(BITS);
-      constexpr int S = fit_stages<BITS, W, E, 1>(LOCO_SGD_STAGES);
+      constexpr int S = fit_stages<BITS, W, E, 1>(LOCO_SGD_STAGES, 0, LOCO_SGD_MIN_CTAS);
       constexpr size_t smem = S * Tile<BITS, W, E, 1>::kBytes;
       static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
       const void* fn = reinterpret_cast<const void*>(&k_sgd<BITS, W, E, S, BF16OUT>);
