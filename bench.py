@@ -62,24 +62,38 @@ def parse():
     ap.add_argument("--param-bf16", action="store_true", help="also write the bf16 copy of the updated parameters")
     ap.add_argument("--fixed-scale", type=float, default=None,
                     help="paper-literal fixed quantisation scale s (e.g. 524288 = 2^19) instead of blockwise absmax")
+    ap.add_argument("--bits", type=int, default=None, choices=[4, 8], help="override the workload's code width")
+    ap.add_argument("--block", type=int, default=None, help="override the workload's scale block (power of two)")
+    ap.add_argument("--ranks", type=int, default=None, help="override the workload's W simulated ranks (1..16)")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="leave out the timed oracle sample (for sweeps; the default run reports it)")
     return ap.parse_args()
 
 
 # ----------------------------------------------------------------------------- workload
 
-def workload(name: str):
+def workload(name: str, bits=None, block=None, ranks=None):
+    """The named workload, with its code width, block or rank count replaced
+    where given (the name then records the change)."""
+    import dataclasses
     from bit_gradient_compression_gb300 import workloads as wl
     if name == "llama2-7b":
-        return wl.LLAMA2_7B
-    if name == "tinyllama":
-        return wl.TINYLLAMA
-    if name == "mixtral":
-        return wl.MIXTRAL_MOE
-    if name.startswith("flat:"):
+        w = wl.LLAMA2_7B
+    elif name == "tinyllama":
+        w = wl.TINYLLAMA
+    elif name == "mixtral":
+        w = wl.MIXTRAL_MOE
+    elif name.startswith("flat:"):
         import torch
         n = 1 << int(name.split(":")[1])
-        return wl.Workload(f"flat-bf16-2^{name.split(':')[1]}", n, torch.bfloat16, 4, 256, 8, 1, "flat")
-    raise SystemExit(f"unknown workload {name}")
+        w = wl.Workload(f"flat-bf16-2^{name.split(':')[1]}", n, torch.bfloat16, 4, 256, 8, 1, "flat")
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    over = {k: v for k, v in (("bits", bits), ("block", block), ("W", ranks)) if v is not None and v != getattr(w, k)}
+    if over:
+        tag = ",".join(f"{k}={v}" for k, v in over.items())
+        w = dataclasses.replace(w, name=f"{w.name}[{tag}]", **over)
+    return w
 
 
 def kernel_bytes(n, gsize, bits, block, W, e8=False, optimizer="adam", bf16_out=False):
@@ -426,7 +440,7 @@ def run_loco(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workload(args.workload)
+    w = workload(args.workload, args.bits, args.block, args.ranks)
     n, bits, block, W = w.n, w.bits, w.block, w.W
     gsize = 2 if w.grad_dtype == torch.bfloat16 else 4
     # beta weights the previous error; the 8-bit storage needs weight on the new error (see loco.h)
@@ -606,7 +620,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        w = workload(args.workload)
+        w = workload(args.workload, args.bits, args.block, args.ranks)
         S = min(w.n, 1 << 25)
         cb = cpu_baseline(w, S, args.steps, args.warmup)
         out = {"impl": "reference", "metric": METRIC, "value": round(cb["value"], 3), "unit": UNIT,
@@ -625,8 +639,11 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     out = run_loco(args, rank, world)
-    if rank == 0:
-        w = workload(args.workload)
+    if rank == 0 and args.no_cpu_baseline:
+        out["cpu_baseline"] = None
+        print(json.dumps(out), flush=True)
+    elif rank == 0:
+        w = workload(args.workload, args.bits, args.block, args.ranks)
         S = min(w.n, 1 << 27)
         try:
             out["cpu_baseline"] = cpu_baseline(w, S, 1, 1, args.optimizer)

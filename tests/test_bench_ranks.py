@@ -48,3 +48,14 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks([3.0, 4.0], "cpu") == [3.0, 4.0]
     assert bench.whole_job_value(2 * 10 ** 9, 1, 1000.0) == pytest.approx(2.0)
+
+
+def test_workload_overrides():
+    import bench
+    w = bench.workload("llama2-7b")
+    assert (w.name, w.n, w.bits, w.block, w.W) == ("llama2-7b-bf16", 6738415616, 4, 256, 8)
+    assert bench.workload("llama2-7b", 4, 256, 8) == w          # overrides equal to the defaults change nothing
+    o = bench.workload("flat:30", bits=8, ranks=16)
+    assert (o.n, o.bits, o.block, o.W) == (1 << 30, 8, 256, 16)
+    assert o.name == "flat-bf16-2^30[bits=8,W=16]"                # a changed config never matches stored counters
+    assert bench.kernel_bytes(1 << 10, 2, 8, 256, 16)["decode_reduce"] == 16 * (1024 + 16) + 4096
