@@ -148,6 +148,7 @@ static loco_status check_ranks(const loco_config* cfg, const uint8_t* const* cod
     out->codes[w] = nullptr;
     out->scales[w] = nullptr;
   }
+  out->neg_zero = -0.0f;
   return LOCO_OK;
 }
 

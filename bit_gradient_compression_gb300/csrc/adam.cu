@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_adam(const AdamArgs a, int log2
           m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
           v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
         }
-        tile_mean<BITS, W, E, 3>(tl, t, log2_block, g);
+        tile_mean<BITS, W, E, 3>(tl, t, log2_block, a.ranks.neg_zero, g);
 #pragma unroll
         for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
         store_vec<E>(a.param, e0, a.n, true, p);

@@ -21,13 +21,26 @@ namespace loco {
 // tile and one bulk copy per tile; with 4-bit codes of more ranks the kernel is
 // bound by the per-code decode work, the extra shared-memory pass costs more
 // than it saves, and threads store directly with a deeper load pipeline.
+#ifndef LOCO_REDUCE_BULK_MAX_W4
+#define LOCO_REDUCE_BULK_MAX_W4 4  // largest rank count whose 4-bit mean goes through the bulk store
+#endif
+#ifndef LOCO_REDUCE_STAGES8
+#define LOCO_REDUCE_STAGES8 2
+#endif
+#ifndef LOCO_REDUCE_STAGES4_BULK
+#define LOCO_REDUCE_STAGES4_BULK 3
+#endif
+#ifndef LOCO_REDUCE_STAGES4_DIRECT
+#define LOCO_REDUCE_STAGES4_DIRECT 4
+#endif
 template <int BITS, int W>
 constexpr bool use_bulk_store() {
-  return BITS == 8 || W <= 4;
+  return BITS == 8 || W <= LOCO_REDUCE_BULK_MAX_W4;
 }
 template <int BITS, int W>
 constexpr int wanted_stages() {
-  return BITS == 8 ? 2 : (use_bulk_store<BITS, W>() ? 3 : 4);
+  return BITS == 8 ? LOCO_REDUCE_STAGES8
+                   : (use_bulk_store<BITS, W>() ? LOCO_REDUCE_STAGES4_BULK : LOCO_REDUCE_STAGES4_DIRECT);
 }
 
 template <int BITS, int W, int E>
@@ -49,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, 
       none, a.ranks, a.n, log2_block,
       [&](const TL& tl, int64_t e0) {
         float mean[E];
-        tile_mean<BITS, W, E, 0>(tl, threadIdx.x, log2_block, mean);
+        tile_mean<BITS, W, E, 0>(tl, threadIdx.x, log2_block, a.ranks.neg_zero, mean);
         if constexpr (BULK) {
           float4* o = reinterpret_cast<float4*>(out + threadIdx.x * E);
 #pragma unroll

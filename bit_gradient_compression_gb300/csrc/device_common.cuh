@@ -122,14 +122,16 @@ __device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, 
 }
 
 // ---------------------------------------------------------------------------
-// Packed fp32 pairs.  add.rn.f32x2 / mul.rn.f32x2 (sm_100+) each round every
-// lane exactly like the scalar add.rn / mul.rn and issue once per pair.  A
-// packed multiply whose result feeds a packed add, however, was measured to be
-// combined into a single fused multiply-add (one rounding) by the code
-// generator even with .rn and -fmad=false.  So packed ops are used only where
-// no product feeds an add: the offset subtraction of the decode (its input
-// comes from a byte permute) and the final scaling by 1/W.  Products and the
-// rank sum use the scalar __fmul_rn / __fadd_rn, which are never contracted.
+// Packed fp32 pairs.  add.rn.f32x2 / mul.rn.f32x2 / fma.rn.f32x2 (sm_100+)
+// each round every lane exactly like the scalar instruction and issue once per
+// pair.  A packed multiply whose result feeds a packed add, however, was
+// measured to be combined into a single fused multiply-add (one rounding) by
+// the code generator even with .rn and -fmad=false.  Where a product feeds a
+// sum, it is therefore formed as fma(a, b, z) with z = -0.0 read at run time:
+// a + (-0) = a for every a (including +0 and -0 under round-to-nearest), so
+// the result is the rounded product, and since z is not known when the code is
+// generated the fma can be neither turned back into a multiply nor merged
+// with the add that follows.  mul2 is used only where no add consumes it.
 // ---------------------------------------------------------------------------
 typedef unsigned long long f32x2;
 
@@ -154,6 +156,12 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
 __device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
   f32x2 r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// Rounded product a * b per lane; neg_zero2 must hold (-0.0f, -0.0f) at run time.
+__device__ __forceinline__ f32x2 prod2(f32x2 a, f32x2 b, f32x2 neg_zero2) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(neg_zero2));
   return r;
 }
 
@@ -231,13 +239,16 @@ struct ChunkCodes {
   }
 };
 
-// Division by W: for a power of two, multiplying by the exact reciprocal gives
-// the same correctly rounded quotient; otherwise an IEEE division.
+// Division by W of a pair of sums: for a power of two, multiplying by the
+// exact reciprocal gives the same correctly rounded quotient; otherwise an
+// IEEE division per lane.
 template <int W>
-__device__ __forceinline__ void div_by_ranks(float a, float b, float& lo, float& hi) {
+__device__ __forceinline__ void div_by_ranks(f32x2 sum, float& lo, float& hi) {
   if constexpr ((W & (W - 1)) == 0) {
-    upk2(mul2(pk2(a, b), pk2(1.0f / float(W), 1.0f / float(W))), lo, hi);
+    upk2(mul2(sum, pk2(1.0f / float(W), 1.0f / float(W))), lo, hi);
   } else {
+    float a, b;
+    upk2(sum, a, b);
     lo = __fdiv_rn(a, float(W));
     hi = __fdiv_rn(b, float(W));
   }
@@ -245,26 +256,26 @@ __device__ __forceinline__ void div_by_ranks(float a, float b, float& lo, float&
 
 // Per-element fp32 rank average of Eqn (8) for an E-element chunk from its
 // W ranks' codes and steps, in rank order 0..W-1:
-//   ((d_0 + d_1) + d_2) + ... , d_w = f32(q_w) * Delta_w, then / W.
+//   ((d_0 + d_1) + d_2) + ... , d_w = f32(q_w) * Delta_w (rounded), then / W.
+// Two elements per instruction: packed products (prod2) and packed sums.
 template <int BITS, int W, int E>
-__device__ __forceinline__ void mean_of_codes(const ChunkCodes<BITS, E> (&cw)[W], const float (&s)[W], float out[E]) {
-  float acc[E];
+__device__ __forceinline__ void mean_of_codes(const ChunkCodes<BITS, E> (&cw)[W], const float (&s)[W], float neg_zero,
+                                              float out[E]) {
+  const f32x2 z = pk2(neg_zero, neg_zero);
+  f32x2 acc[E / 2];
 #pragma unroll
   for (int w = 0; w < W; ++w) {
     f32x2 q2[E / 2];
     cw[w].decode(q2);
+    const f32x2 s2 = pk2(s[w], s[w]);
 #pragma unroll
     for (int j = 0; j < E / 2; ++j) {
-      float qa, qb;
-      upk2(q2[j], qa, qb);
-      const float da = __fmul_rn(qa, s[w]);
-      const float db = __fmul_rn(qb, s[w]);
-      acc[2 * j] = (w == 0) ? da : __fadd_rn(acc[2 * j], da);
-      acc[2 * j + 1] = (w == 0) ? db : __fadd_rn(acc[2 * j + 1], db);
+      const f32x2 d = prod2(q2[j], s2, z);
+      acc[j] = (w == 0) ? d : add2(acc[j], d);
     }
   }
 #pragma unroll
-  for (int j = 0; j < E / 2; ++j) div_by_ranks<W>(acc[2 * j], acc[2 * j + 1], out[2 * j], out[2 * j + 1]);
+  for (int j = 0; j < E / 2; ++j) div_by_ranks<W>(acc[j], out[2 * j], out[2 * j + 1]);
 }
 
 // Same, loading the codes straight from global memory (chunk at e0, block blk).
@@ -277,7 +288,7 @@ __device__ __forceinline__ void decode_mean(const RankPtrs& rp, int64_t e0, int6
     cw[w].load(rp.codes[w], e0);
     s[w] = __ldg(rp.scales[w] + blk);
   }
-  mean_of_codes<BITS, W, E>(cw, s, out);
+  mean_of_codes<BITS, W, E>(cw, s, rp.neg_zero, out);
 }
 
 }  // namespace loco

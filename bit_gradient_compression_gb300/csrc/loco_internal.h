@@ -33,6 +33,10 @@ struct CompressArgs {
 struct RankPtrs {
   const uint8_t* codes[kMaxRanks];
   const float* scales[kMaxRanks];
+  // -0.0f, passed at run time: the addend of the packed product q * Delta
+  // (fma(q, Delta, -0) rounds exactly like the product, and a value the code
+  // generator cannot see keeps it from merging the product into the rank sum).
+  float neg_zero;
 };
 
 struct ReduceArgs {

@@ -104,7 +104,8 @@ __device__ __forceinline__ void issue_tile(const Tile<BITS, W, E, NF>& dst, cons
 
 // Rank average of this thread's E elements of a staged tile.
 template <int BITS, int W, int E, int NF>
-__device__ __forceinline__ void tile_mean(const Tile<BITS, W, E, NF>& tl, int t, int log2_block, float out[E]) {
+__device__ __forceinline__ void tile_mean(const Tile<BITS, W, E, NF>& tl, int t, int log2_block, float neg_zero,
+                                          float out[E]) {
   ChunkCodes<BITS, E> cw[W];
   float sc[W];
   const int blk = (t * E) >> log2_block;
@@ -113,7 +114,7 @@ __device__ __forceinline__ void tile_mean(const Tile<BITS, W, E, NF>& tl, int t,
     cw[w].load_shared(tl.codes(w) + (t * E * BITS >> 3));
     sc[w] = tl.scales(w)[blk];
   }
-  mean_of_codes<BITS, W, E>(cw, sc, out);
+  mean_of_codes<BITS, W, E>(cw, sc, neg_zero, out);
 }
 
 // Receiver tiles through the multistage pipeline; elements past the last full

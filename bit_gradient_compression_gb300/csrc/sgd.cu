@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kThreads) k_sgd(const SgdArgs a, int log2_bloc
           const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
           p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
         }
-        tile_mean<BITS, W, E, 1>(tl, t, log2_block, g);
+        tile_mean<BITS, W, E, 1>(tl, t, log2_block, a.ranks.neg_zero, g);
 #pragma unroll
         for (int j = 0; j < E; ++j) p[j] = __fsub_rn(p[j], __fmul_rn(a.lr, g[j]));
         store_vec<E>(a.param, e0, a.n, true, p);
