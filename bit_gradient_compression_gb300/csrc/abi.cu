@@ -240,7 +240,15 @@ static loco_status compress_common(const loco_config* cfg, const void* grad, int
   a.beta = cfg->beta;
   a.one_minus_beta = 1.0f - cfg->beta;
   a.kappa = cfg->err_scale_mult;
+  {
+    // A power of two 2^k with 2^-k a normal float: dividing by it is the same
+    // real as multiplying by its exact reciprocal, so both round alike.
+    int ex = 0;
+    const float m = frexpf(a.kappa, &ex);
+    a.kappa_recip = (m == 0.5f && ex - 1 >= -126 && ex - 1 <= 126) ? ldexpf(1.0f, 1 - ex) : 0.0f;
+  }
   a.reset = cfg->reset_period > 0 && (step % cfg->reset_period) == 0;
+  a.neg_zero = -0.0f;
   return launch_result(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)),
                        e8 ? "loco_compress_e8" : "loco_compress");
 }

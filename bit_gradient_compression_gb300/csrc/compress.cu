@@ -6,40 +6,70 @@
 // the error as a clipped moving average of the compression error, reset every
 // T_c steps.
 //
-// Mapping: one lane owns 8 consecutive elements (one 16-byte load of bf16
-// gradient or two of fp32, two 16-byte loads of the error); a quant block of
-// B elements spans B/8 consecutive lanes, so its absmax is a butterfly of
-// B/8-lane __shfl_xor_sync steps (max is exact, so the order is irrelevant).
-// A warp covers 256 elements.  With only two input streams, direct 16-byte
-// loads from enough resident warps keep HBM busy (a shared-memory staged
-// variant measured slower: its barriers cost more than it hid).  One pass
-// over HBM: read g and e, write e, the packed codes and one step per block.
-// No shared memory, no atomics, no inter-CTA communication.
+// Mapping: one lane owns EL consecutive elements (8 with the fp32 error: one
+// 16-byte load of bf16 gradient or two of fp32, two of the error; 16 with the
+// int8 error, whose path is bound by instruction issue rather than HBM); a
+// quant block of B elements spans B/EL consecutive lanes, so its absmax is a
+// butterfly of __shfl_xor_sync steps (max is exact, so the order is
+// irrelevant), and a warp covers 32*EL elements.  With 16 elements per lane a
+// warp spans two 256-element blocks whose scales its half-warps compute in the
+// same instructions, which halves the per-element cost of the three IEEE
+// divisions.  The fp32 arithmetic runs on packed pairs (f32x2).  With only two
+// input streams, direct vector loads from enough resident warps keep HBM busy
+// (a shared-memory staged variant measured slower: its barriers cost more than
+// it hid).  One pass over HBM: read g and e, write e, the packed codes and one
+// step per block.  No shared memory, no atomics, no inter-CTA communication.
 #include "device_common.cuh"
 
 namespace loco {
 
 constexpr int kThreads = 256;
 
-// Eqns (2),(1),(3),(4),(5),(7) for the 8 elements [e0, e0+8) of one lane,
-// given their gradient g and previous error e (0 past n).  All 32 lanes of the
-// warp must call this together (the absmax is a warp shuffle).  E8 selects
-// the 8-bit error storage: the new error is written as int8 codes of step
-// Delta/kappa instead of clipped fp32 values.
-template <int BITS, int BLOCK, bool E8, bool FIXED>
-__device__ __forceinline__ void compress8(const CompressArgs& a, int64_t e0, int64_t n_pad, int lane, const float g[8],
-                                          const float e[8]) {
-  constexpr int G = BLOCK / 8;  // lanes per quant block
+// Stores NW consecutive 32-bit words with one streaming store (NW = 1, 2, 4).
+template <int NW>
+__device__ __forceinline__ void st_words(void* p, const uint32_t (&w)[NW]) {
+  static_assert(NW == 1 || NW == 2 || NW == 4, "one 4-, 8- or 16-byte store");
+  if constexpr (NW == 1)
+    st_stream(reinterpret_cast<uint32_t*>(p), w[0]);
+  else if constexpr (NW == 2)
+    st_stream(reinterpret_cast<uint2*>(p), make_uint2(w[0], w[1]));
+  else
+    st_stream(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
+}
+
+// Low bytes of four words, in order, as one word.
+__device__ __forceinline__ uint32_t low_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
+// Eqns (2),(1),(3),(4),(5),(7) for the EL elements [e0, e0+EL) of one lane,
+// given their gradient g and previous error e as EL/2 packed pairs (element
+// 2k in the low lane of pair k; 0 past n).  All 32 lanes of the warp must call
+// this together (the absmax is a warp shuffle over the BLOCK/EL lanes of a
+// block).  E8 selects the 8-bit error storage: the new error is written as
+// int8 codes of step Delta/kappa instead of clipped fp32 values.  Every fp32
+// multiply and add is one packed instruction per pair with the rounding of the
+// scalar one; products that feed an add are formed by prod2.
+template <int BITS, int BLOCK, bool E8, bool FIXED, int EL>
+__device__ __forceinline__ void compress_chunk(const CompressArgs& a, int64_t e0, int64_t n_pad, int lane,
+                                               const f32x2 (&g)[EL / 2], const f32x2 (&e)[EL / 2]) {
+  constexpr int P = EL / 2;     // pairs per lane
+  constexpr int G = BLOCK / EL;  // lanes per quant block
+  static_assert(EL == 8 || EL == 16, "8 or 16 elements per lane");
+  static_assert(G >= 1 && G <= 32 && BLOCK % EL == 0, "a lane's elements lie in one block");
   constexpr float QMAX = float((1 << (BITS - 1)) - 1);
   constexpr float QMIN = -float(1 << (BITS - 1));
+  const f32x2 z = pk2(a.neg_zero, a.neg_zero);
 
   // Eqn (2): compensate; block absmax.
-  float h[8];
+  f32x2 h[P];
   float amax = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    h[j] = __fadd_rn(g[j], e[j]);
-    amax = fmaxf(amax, fabsf(h[j]));
+  for (int k = 0; k < P; ++k) {
+    h[k] = add2(g[k], e[k]);
+    float h0, h1;
+    upk2(h[k], h0, h1);
+    amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
   }
 #pragma unroll
   for (int off = G / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -60,305 +90,280 @@ __device__ __forceinline__ void compress8(const CompressArgs& a, int64_t e0, int
       delta = __fdiv_rn(amax, QMAX);
     }
   }
-  const float de = __fdiv_rn(delta, a.kappa);
+  const float de = (a.kappa_recip != 0.0f) ? __fmul_rn(delta, a.kappa_recip) : __fdiv_rn(delta, a.kappa);
   const float elo = __fmul_rn(-128.0f, de);
   const float ehi = __fmul_rn(127.0f, de);
   float inv_e = __fmul_rn(a.kappa, inv);  // s_e = kappa * s; code 0 if it overflows
   if (isinf(inv_e)) inv_e = 0.0f;
 
-  // Eqns (1),(3),(4),(5),(7) per element.  tq / teq hold the float whose low
+  // Eqns (1),(3),(4),(5),(7) per pair.  tq / teq hold the float whose low
   // byte is the two's-complement code (1.5*2^23 + q).
-  uint32_t tq[8], teq[8];
-  float en[8];
+  const f32x2 inv2 = pk2(inv, inv), delta2 = pk2(delta, delta), inv_e2 = pk2(inv_e, inv_e);
+  const f32x2 magic2 = pk2(kRoundMagic, kRoundMagic);
+  const f32x2 beta2 = pk2(a.beta, a.beta), omb2 = pk2(a.one_minus_beta, a.one_minus_beta);
+  uint32_t tq[EL], teq[EL];
+  float en[EL];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float x = __fmul_rn(h[j], inv);
+  for (int k = 0; k < P; ++k) {
+    f32x2 x = prod2(h[k], inv2, z);
     // Saturation of Round_p-bit.  With the absmax step it is a no-op for finite
     // inputs: |h| <= A and inv = RN(qmax/A) give |x| <= qmax*(1 + 2^-23) < qmax + 1/2,
     // which rounds to at most qmax; only a fixed scale can push x past the range.
-    if constexpr (FIXED) x = fminf(fmaxf(x, QMIN), QMAX);
-    const float t = __fadd_rn(x, kRoundMagic);  // rint, halves to even
-    tq[j] = __float_as_uint(t);
-    const float q = __fsub_rn(t, kRoundMagic);
-    const float d = __fmul_rn(q, delta);
-    const float r = __fsub_rn(h[j], d);
-    float v = __fadd_rn(__fmul_rn(a.beta, e[j]), __fmul_rn(a.one_minus_beta, r));
+    if constexpr (FIXED) {
+      float x0, x1;
+      upk2(x, x0, x1);
+      x = pk2(fminf(fmaxf(x0, QMIN), QMAX), fminf(fmaxf(x1, QMIN), QMAX));
+    }
+    const f32x2 t = add2(x, magic2);  // rint, halves to even
+    float t0, t1;
+    upk2(t, t0, t1);
+    tq[2 * k] = __float_as_uint(t0);
+    tq[2 * k + 1] = __float_as_uint(t1);
+    const f32x2 q = sub2(t, magic2);
+    const f32x2 r = sub2(h[k], prod2(q, delta2, z));
+    const f32x2 v = add2(prod2(beta2, e[k], z), prod2(omb2, r, z));
+    float v0, v1;
     if constexpr (E8) {
       // Eqn (7): e = Round_8-bit(s_e * e~).
-      float xe = __fmul_rn(v, inv_e);
-      xe = fminf(fmaxf(xe, -128.0f), 127.0f);
-      teq[j] = __float_as_uint(__fadd_rn(xe, kRoundMagic));
+      upk2(prod2(v, inv_e2, z), v0, v1);
+      const f32x2 te = add2(pk2(fminf(fmaxf(v0, -128.0f), 127.0f), fminf(fmaxf(v1, -128.0f), 127.0f)), magic2);
+      float te0, te1;
+      upk2(te, te0, te1);
+      teq[2 * k] = __float_as_uint(te0);
+      teq[2 * k + 1] = __float_as_uint(te1);
     } else {
-      v = (v < elo) ? elo : v;
-      v = (v > ehi) ? ehi : v;
-      en[j] = v;
+      upk2(v, v0, v1);
+      v0 = (v0 < elo) ? elo : v0;
+      v0 = (v0 > ehi) ? ehi : v0;
+      v1 = (v1 < elo) ? elo : v1;
+      v1 = (v1 > ehi) ? ehi : v1;
+      en[2 * k] = v0;
+      en[2 * k + 1] = v1;
     }
   }
   // Reset step of Eqn (7): the stored error becomes 0 (a uniform branch).
   if (a.reset) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < EL; ++j) {
       en[j] = 0.0f;
       teq[j] = 0u;
     }
   }
   // Pack the low bytes / nibbles with byte permutes.
-  uint32_t packed[BITS == 4 ? 1 : 2];
-  if constexpr (BITS == 8) {
-    packed[0] = __byte_perm(__byte_perm(tq[0], tq[1], 0x0040), __byte_perm(tq[2], tq[3], 0x0040), 0x5410);
-    packed[1] = __byte_perm(__byte_perm(tq[4], tq[5], 0x0040), __byte_perm(tq[6], tq[7], 0x0040), 0x5410);
-  } else {
-    // byte k = (code_{2k} & 0xF) | (code_{2k+1} << 4)
-    uint32_t b[4];
+  constexpr int CW = EL * BITS / 32;  // code words per lane
+  uint32_t packed[CW];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) b[k] = (tq[2 * k] & 0xFu) | ((tq[2 * k + 1] << 4) & 0xF0u);
-    packed[0] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
-  }
-  uint32_t epacked[2] = {0u, 0u};
-  if constexpr (E8) {
-    epacked[0] = __byte_perm(__byte_perm(teq[0], teq[1], 0x0040), __byte_perm(teq[2], teq[3], 0x0040), 0x5410);
-    epacked[1] = __byte_perm(__byte_perm(teq[4], teq[5], 0x0040), __byte_perm(teq[6], teq[7], 0x0040), 0x5410);
+  for (int w = 0; w < CW; ++w) {
+    if constexpr (BITS == 8) {
+      packed[w] = low_bytes(tq[4 * w], tq[4 * w + 1], tq[4 * w + 2], tq[4 * w + 3]);
+    } else {
+      // byte k = (code_{2k} & 0xF) | (code_{2k+1} << 4): gather the even and odd
+      // codes' low bytes, then merge the two words nibble-wise.
+      const uint32_t* c = tq + 8 * w;
+      const uint32_t ev = low_bytes(c[0], c[2], c[4], c[6]);
+      const uint32_t od = low_bytes(c[1], c[3], c[5], c[7]);
+      packed[w] = (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
+    }
   }
 
   // Stores: codes and the block step inside the padded code range, the error
   // only for elements < n.
   if (e0 < n_pad) {
-    if constexpr (BITS == 4)
-      st_stream(reinterpret_cast<uint32_t*>(a.codes + (e0 >> 1)), packed[0]);
-    else
-      st_stream(reinterpret_cast<uint2*>(a.codes + e0), make_uint2(packed[0], packed[1]));
+    st_words<CW>(a.codes + (e0 * BITS >> 3), packed);
     if ((lane & (G - 1)) == 0) {
       a.scales[e0 / BLOCK] = delta;
       if constexpr (E8) a.err_steps[e0 / BLOCK] = de;
     }
   }
   if constexpr (E8) {
-    if (e0 + 8 <= a.n) {
-      st_stream(reinterpret_cast<uint2*>(a.err_codes + e0), make_uint2(epacked[0], epacked[1]));
+    uint32_t epacked[EL / 4];
+#pragma unroll
+    for (int w = 0; w < EL / 4; ++w) epacked[w] = low_bytes(teq[4 * w], teq[4 * w + 1], teq[4 * w + 2], teq[4 * w + 3]);
+    if (e0 + EL <= a.n) {
+      st_words<EL / 4>(a.err_codes + e0, epacked);
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < EL; ++j)
         if (e0 + j < a.n) a.err_codes[e0 + j] = int8_t((epacked[j >> 2] >> (8 * (j & 3))) & 0xFFu);
     }
-  } else if (e0 + 8 <= a.n) {
+  } else if (e0 + EL <= a.n) {
     float4* ep = reinterpret_cast<float4*>(a.err + e0);
-    st_stream(ep, make_float4(en[0], en[1], en[2], en[3]));
-    st_stream(ep + 1, make_float4(en[4], en[5], en[6], en[7]));
+#pragma unroll
+    for (int i = 0; i < EL / 4; ++i) st_stream(ep + i, make_float4(en[4 * i], en[4 * i + 1], en[4 * i + 2], en[4 * i + 3]));
   } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < EL; ++j)
       if (e0 + j < a.n) a.err[e0 + j] = en[j];
   }
 }
 
-// Loads the 8 gradient values of the lane's chunk at e0 (0 past n).
-template <bool BF16>
-__device__ __forceinline__ void load_grad8(const CompressArgs& a, int64_t e0, float g[8]) {
-  if (e0 + 8 <= a.n) {
-    if constexpr (BF16) {
-      const uint4 raw = ld_stream(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.grad) + e0));
-      g[0] = bf16lo_to_f32(raw.x); g[1] = bf16hi_to_f32(raw.x);
-      g[2] = bf16lo_to_f32(raw.y); g[3] = bf16hi_to_f32(raw.y);
-      g[4] = bf16lo_to_f32(raw.z); g[5] = bf16hi_to_f32(raw.z);
-      g[6] = bf16lo_to_f32(raw.w); g[7] = bf16hi_to_f32(raw.w);
-    } else {
-      const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(a.grad) + e0);
-      const float4 g0 = ld_stream(gp), g1 = ld_stream(gp + 1);
-      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-      g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-    }
-  } else {
+// Gradient and error of a lane chunk that crosses n, element by element (0
+// past n).  With E8 the previous error is decoded from its int8 code and the
+// block's stored step: e = f32(qe) * De (the decompressor of Eqn 2).
+template <bool BF16, bool E8, int BLOCK, int EL>
+__device__ __forceinline__ void load_partial(const CompressArgs& a, int64_t e0, f32x2 (&g)[EL / 2],
+                                             f32x2 (&e)[EL / 2]) {
+  float gs[EL], es[EL];
+  const float dprev = (E8 && e0 < a.n) ? a.err_steps[e0 / BLOCK] : 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int64_t i = e0 + j;
-      if (i < a.n) {
-        if constexpr (BF16)
-          g[j] = __uint_as_float(uint32_t(static_cast<const uint16_t*>(a.grad)[i]) << 16);
-        else
-          g[j] = static_cast<const float*>(a.grad)[i];
-      } else {
-        g[j] = 0.0f;
-      }
+  for (int j = 0; j < EL; ++j) {
+    const int64_t i = e0 + j;
+    gs[j] = 0.0f;
+    es[j] = 0.0f;
+    if (i < a.n) {
+      if constexpr (BF16)
+        gs[j] = __uint_as_float(uint32_t(static_cast<const uint16_t*>(a.grad)[i]) << 16);
+      else
+        gs[j] = static_cast<const float*>(a.grad)[i];
+      if constexpr (E8)
+        es[j] = __fmul_rn(float(a.err_codes[i]), dprev);
+      else
+        es[j] = a.err[i];
     }
+  }
+#pragma unroll
+  for (int k = 0; k < EL / 2; ++k) {
+    g[k] = pk2(gs[2 * k], gs[2 * k + 1]);
+    e[k] = pk2(es[2 * k], es[2 * k + 1]);
   }
 }
 
-// Loads the 8 gradient and error values of the lane's chunk at e0 (0 past n).
-// With E8 the previous error is decoded from its int8 codes and the block's
-// stored step: e = f32(qe) * De (the decompressor of Eqn 2).
-template <bool BF16, bool E8, int BLOCK>
-__device__ __forceinline__ void load8(const CompressArgs& a, int64_t e0, float g[8], float e[8]) {
-  if constexpr (E8) {
-    load_grad8<BF16>(a, e0, g);
-    const float dprev = (e0 < a.n) ? a.err_steps[e0 / BLOCK] : 0.0f;
-    uint32_t w0 = 0, w1 = 0;
-    if (e0 + 8 <= a.n) {
-      const uint2 v = ld_stream(reinterpret_cast<const uint2*>(a.err_codes + e0));
-      w0 = v.x;
-      w1 = v.y;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t b = (e0 + j < a.n) ? uint32_t(uint8_t(a.err_codes[e0 + j])) : 0u;
-        if (j < 4) w0 |= b << (8 * j); else w1 |= b << (8 * (j - 4));
-      }
-    }
-    constexpr uint32_t K = 0x4B000000u;
-    const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float q0 = __fsub_rn(__uint_as_float(__byte_perm(u0, K, 0x7440 | j)), 8388736.0f);
-      const float q1 = __fsub_rn(__uint_as_float(__byte_perm(u1, K, 0x7440 | j)), 8388736.0f);
-      e[j] = __fmul_rn(q0, dprev);
-      e[j + 4] = __fmul_rn(q1, dprev);
-    }
-    return;
-  }
-  if (e0 + 8 <= a.n) {
-    if constexpr (BF16) {
-      const uint4 raw = ld_stream(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.grad) + e0));
-      g[0] = bf16lo_to_f32(raw.x); g[1] = bf16hi_to_f32(raw.x);
-      g[2] = bf16lo_to_f32(raw.y); g[3] = bf16hi_to_f32(raw.y);
-      g[4] = bf16lo_to_f32(raw.z); g[5] = bf16hi_to_f32(raw.z);
-      g[6] = bf16lo_to_f32(raw.w); g[7] = bf16hi_to_f32(raw.w);
-    } else {
-      const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(a.grad) + e0);
-      const float4 g0 = ld_stream(gp), g1 = ld_stream(gp + 1);
-      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-      g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-    }
-    const float4* ep = reinterpret_cast<const float4*>(a.err + e0);
-    const float4 e0v = ld_stream(ep), e1v = ld_stream(ep + 1);
-    e[0] = e0v.x; e[1] = e0v.y; e[2] = e0v.z; e[3] = e0v.w;
-    e[4] = e1v.x; e[5] = e1v.y; e[6] = e1v.z; e[7] = e1v.w;
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int64_t i = e0 + j;
-      if (i < a.n) {
-        if constexpr (BF16)
-          g[j] = __uint_as_float(uint32_t(static_cast<const uint16_t*>(a.grad)[i]) << 16);
-        else
-          g[j] = static_cast<const float*>(a.grad)[i];
-        e[j] = a.err[i];
-      } else {
-        g[j] = 0.0f;
-        e[j] = 0.0f;
-      }
-    }
-  }
-}
-
-// Raw words of one lane's full 8-element chunk, loaded with 16- or 8-byte
-// vector loads and decoded only when the chunk is processed, so several
-// chunks can be in flight in few registers.  8-bit error storage keeps the
-// codes in e[0].x/.y and the block's stored step in e[0].z.
-template <bool BF16, bool E8>
+// Raw words of one lane's full EL-element chunk, loaded with 16-byte (or, for
+// 8 int8 codes, 8-byte) vector loads and decoded only when the chunk is
+// processed, so several chunks can be in flight in few registers.
+template <bool BF16, bool E8, int EL>
 struct RawChunk {
-  uint4 g[BF16 ? 1 : 2];
-  uint4 e[E8 ? 1 : 2];
+  static constexpr int kG = EL * (BF16 ? 2 : 4) / 16;  // 16-byte words of gradient
+  uint4 g[kG];
+  uint4 e[E8 ? 1 : EL / 4];  // fp32 error, or the int8 codes in the first EL/4 words
+  float step;                // block step of the int8 codes
 };
 
-template <bool BF16, bool E8, int BLOCK>
-__device__ __forceinline__ void load_raw(const CompressArgs& a, int64_t e0, RawChunk<BF16, E8>& r) {
+template <bool BF16, bool E8, int BLOCK, int EL>
+__device__ __forceinline__ void load_raw(const CompressArgs& a, int64_t e0, RawChunk<BF16, E8, EL>& r) {
   const uint4* gp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.grad) + e0 * (BF16 ? 2 : 4));
-  r.g[0] = ld_stream(gp);
-  if constexpr (!BF16) r.g[1] = ld_stream(gp + 1);
+#pragma unroll
+  for (int i = 0; i < RawChunk<BF16, E8, EL>::kG; ++i) r.g[i] = ld_stream(gp + i);
   if constexpr (E8) {
-    const uint2 c = ld_stream(reinterpret_cast<const uint2*>(a.err_codes + e0));
-    r.e[0] = make_uint4(c.x, c.y, __float_as_uint(a.err_steps[e0 / BLOCK]), 0u);
+    if constexpr (EL == 16) {
+      r.e[0] = ld_stream(reinterpret_cast<const uint4*>(a.err_codes + e0));
+    } else {
+      const uint2 c = ld_stream(reinterpret_cast<const uint2*>(a.err_codes + e0));
+      r.e[0] = make_uint4(c.x, c.y, 0u, 0u);
+    }
+    r.step = a.err_steps[e0 / BLOCK];
   } else {
     const uint4* ep = reinterpret_cast<const uint4*>(a.err + e0);
-    r.e[0] = ld_stream(ep);
-    r.e[1] = ld_stream(ep + 1);
+#pragma unroll
+    for (int i = 0; i < EL / 4; ++i) r.e[i] = ld_stream(ep + i);
   }
 }
 
-template <bool BF16, bool E8>
-__device__ __forceinline__ void unpack_raw(const RawChunk<BF16, E8>& r, float g[8], float e[8]) {
-  if constexpr (BF16) {
-    g[0] = bf16lo_to_f32(r.g[0].x); g[1] = bf16hi_to_f32(r.g[0].x);
-    g[2] = bf16lo_to_f32(r.g[0].y); g[3] = bf16hi_to_f32(r.g[0].y);
-    g[4] = bf16lo_to_f32(r.g[0].z); g[5] = bf16hi_to_f32(r.g[0].z);
-    g[6] = bf16lo_to_f32(r.g[0].w); g[7] = bf16hi_to_f32(r.g[0].w);
-  } else {
+template <bool BF16, bool E8, int EL>
+__device__ __forceinline__ void unpack_raw(const RawChunk<BF16, E8, EL>& r, float neg_zero, f32x2 (&g)[EL / 2],
+                                           f32x2 (&e)[EL / 2]) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      g[4 * i] = __uint_as_float(r.g[i].x); g[4 * i + 1] = __uint_as_float(r.g[i].y);
-      g[4 * i + 2] = __uint_as_float(r.g[i].z); g[4 * i + 3] = __uint_as_float(r.g[i].w);
+  for (int i = 0; i < RawChunk<BF16, E8, EL>::kG; ++i) {
+    const uint32_t wv[4] = {r.g[i].x, r.g[i].y, r.g[i].z, r.g[i].w};
+    if constexpr (BF16) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) g[4 * i + c] = pk2(bf16lo_to_f32(wv[c]), bf16hi_to_f32(wv[c]));
+    } else {
+      g[2 * i] = pk2u(wv[0], wv[1]);
+      g[2 * i + 1] = pk2u(wv[2], wv[3]);
     }
   }
   if constexpr (E8) {
+    // e = f32(qe) * De: biased floats 2^23 + 128 + qe from byte permutes, the
+    // offset subtracted exactly, then the rounded product.
     constexpr uint32_t K = 0x4B000000u;
-    const uint32_t u0 = r.e[0].x ^ 0x80808080u, u1 = r.e[0].y ^ 0x80808080u;
-    const float dprev = __uint_as_float(r.e[0].z);
+    const uint32_t cw[4] = {r.e[0].x, r.e[0].y, r.e[0].z, r.e[0].w};
+    const f32x2 off = pk2(8388736.0f, 8388736.0f), dp = pk2(r.step, r.step), z = pk2(neg_zero, neg_zero);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      e[j] = __fmul_rn(__fsub_rn(__uint_as_float(__byte_perm(u0, K, 0x7440 | j)), 8388736.0f), dprev);
-      e[j + 4] = __fmul_rn(__fsub_rn(__uint_as_float(__byte_perm(u1, K, 0x7440 | j)), 8388736.0f), dprev);
+    for (int w = 0; w < EL / 4; ++w) {
+      const uint32_t u = cw[w] ^ 0x80808080u;
+      e[2 * w] = prod2(sub2(pk2u(__byte_perm(u, K, 0x7440), __byte_perm(u, K, 0x7441)), off), dp, z);
+      e[2 * w + 1] = prod2(sub2(pk2u(__byte_perm(u, K, 0x7442), __byte_perm(u, K, 0x7443)), off), dp, z);
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      e[4 * i] = __uint_as_float(r.e[i].x); e[4 * i + 1] = __uint_as_float(r.e[i].y);
-      e[4 * i + 2] = __uint_as_float(r.e[i].z); e[4 * i + 3] = __uint_as_float(r.e[i].w);
+    for (int i = 0; i < EL / 4; ++i) {
+      e[2 * i] = pk2u(r.e[i].x, r.e[i].y);
+      e[2 * i + 1] = pk2u(r.e[i].z, r.e[i].w);
     }
   }
 }
 
-// Warps walk the bucket's 256-element warp tiles grid-stride, U tiles per
-// iteration with all their loads issued before any compute; every lane of a
-// warp takes the same trip count, so the shuffles are always full-warp.  A
+// Loads of warp tile t for this lane (a full chunk below n only).
+template <bool BF16, bool E8, int BLOCK, int EL>
+__device__ __forceinline__ void issue_tile(const CompressArgs& a, int64_t t, int64_t ntiles, int lane,
+                                           RawChunk<BF16, E8, EL>& r) {
+  const int64_t e0 = t * (32 * EL) + lane * EL;
+  if (t < ntiles && e0 + EL <= a.n) load_raw<BF16, E8, BLOCK, EL>(a, e0, r);
+}
+
+// Compress this lane's chunk of warp tile t from its loaded words (or, for a
+// chunk that crosses n, element by element).
+template <int BITS, int BLOCK, bool BF16, bool E8, bool FIXED, int EL>
+__device__ __forceinline__ void process_tile(const CompressArgs& a, int64_t t, int64_t n_pad, int lane,
+                                             const RawChunk<BF16, E8, EL>& r) {
+  const int64_t e0 = t * (32 * EL) + lane * EL;
+  f32x2 g[EL / 2], e[EL / 2];
+  if (e0 + EL <= a.n)
+    unpack_raw<BF16, E8, EL>(r, a.neg_zero, g, e);
+  else
+    load_partial<BF16, E8, BLOCK, EL>(a, e0, g, e);
+  compress_chunk<BITS, BLOCK, E8, FIXED, EL>(a, e0, n_pad, lane, g, e);
+}
+
+// Warps walk the bucket's warp tiles (32*EL elements) grid-stride, U tiles
+// per iteration with all their loads issued before any compute; every lane of
+// a warp takes the same trip count, so the shuffles are always full-warp.  A
 // lane whose chunk crosses n (only in the last warp tile) loads it element by
-// element instead.
-template <int BITS, int BLOCK, bool BF16, bool E8, bool FIXED, int U>
+// element instead.  The register budget is the compiler's default for 256
+// threads (a minimum-CTA launch bound lets it grow and costs occupancy).
+template <int BITS, int BLOCK, bool BF16, bool E8, bool FIXED, int U, int EL>
 __global__ void __launch_bounds__(kThreads) k_compress(const CompressArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t nb = (a.n + BLOCK - 1) / BLOCK;
   const int64_t n_pad = nb * BLOCK;
-  const int64_t ntiles = (n_pad + 255) / 256;
+  const int64_t ntiles = (n_pad + 32 * EL - 1) / (32 * EL);
   const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   for (int64_t tile = warp0; tile < ntiles; tile += U * nwarps) {
-    RawChunk<BF16, E8> raw[U];
+    RawChunk<BF16, E8, EL> raw[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t e0 = (tile + u * nwarps) * 256 + lane * 8;
-      if (tile + u * nwarps < ntiles && e0 + 8 <= a.n) load_raw<BF16, E8, BLOCK>(a, e0, raw[u]);
-    }
+    for (int u = 0; u < U; ++u) issue_tile<BF16, E8, BLOCK, EL>(a, tile + u * nwarps, ntiles, lane, raw[u]);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t tu = tile + u * nwarps;
-      if (tu < ntiles) {
-        const int64_t e0 = tu * 256 + lane * 8;
-        float g[8], e[8];
-        if (e0 + 8 <= a.n)
-          unpack_raw<BF16, E8>(raw[u], g, e);
-        else
-          load8<BF16, E8, BLOCK>(a, e0, g, e);
-        compress8<BITS, BLOCK, E8, FIXED>(a, e0, n_pad, lane, g, e);
-      }
-    }
+    for (int u = 0; u < U; ++u)
+      if (tile + u * nwarps < ntiles) process_tile<BITS, BLOCK, BF16, E8, FIXED, EL>(a, tile + u * nwarps, n_pad, lane, raw[u]);
   }
 }
 
 #ifndef LOCO_COMPRESS_UNROLL
 #define LOCO_COMPRESS_UNROLL 2     // fp32 error: 48 bytes per lane per warp tile
 #endif
+#ifndef LOCO_COMPRESS_ELEMS
+#define LOCO_COMPRESS_ELEMS 8      // fp32 error: elements per lane (memory-bound)
+#endif
 #ifndef LOCO_COMPRESS_UNROLL_E8
-#define LOCO_COMPRESS_UNROLL_E8 2  // 8-bit error: 24 bytes per lane per warp tile (issue-bound)
+#define LOCO_COMPRESS_UNROLL_E8 1  // 8-bit error: warp tiles per iteration (64 registers: 4 CTAs per SM)
+#endif
+#ifndef LOCO_COMPRESS_ELEMS_E8
+#define LOCO_COMPRESS_ELEMS_E8 16  // 8-bit error: elements per lane; the half-warps compute two blocks' scales at once
 #endif
 
 template <int BITS, int BLOCK, bool BF16, bool E8, bool FIXED>
 static cudaError_t launch_t(const CompressArgs& a, cudaStream_t s) {
   constexpr int U = E8 ? LOCO_COMPRESS_UNROLL_E8 : LOCO_COMPRESS_UNROLL;
-  const void* fn = reinterpret_cast<const void*>(&k_compress<BITS, BLOCK, BF16, E8, FIXED, U>);
+  constexpr int EL = E8 ? LOCO_COMPRESS_ELEMS_E8 : LOCO_COMPRESS_ELEMS;
+  const void* fn = reinterpret_cast<const void*>(&k_compress<BITS, BLOCK, BF16, E8, FIXED, U, EL>);
   static const int cap = persistent_grid(fn, kThreads);
   const int64_t nb = (a.n + BLOCK - 1) / BLOCK;
-  const int64_t warps_needed = (nb * BLOCK + 255) / 256;
+  const int64_t warps_needed = (nb * BLOCK + 32 * EL - 1) / (32 * EL);
   const int64_t ctas_needed = (warps_needed + kThreads / 32 - 1) / (kThreads / 32);
   const int grid = int(ctas_needed < cap ? ctas_needed : cap);
-  k_compress<BITS, BLOCK, BF16, E8, FIXED, U><<<grid, kThreads, 0, s>>>(a);
+  k_compress<BITS, BLOCK, BF16, E8, FIXED, U, EL><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

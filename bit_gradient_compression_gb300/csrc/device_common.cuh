@@ -158,6 +158,11 @@ __device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 // Rounded product a * b per lane; neg_zero2 must hold (-0.0f, -0.0f) at run time.
 __device__ __forceinline__ f32x2 prod2(f32x2 a, f32x2 b, f32x2 neg_zero2) {
   f32x2 r;

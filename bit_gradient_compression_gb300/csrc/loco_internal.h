@@ -27,7 +27,9 @@ struct CompressArgs {
   float beta;
   float one_minus_beta;  // 1 - beta, formed once in fp32
   float kappa;
+  float kappa_recip;  // 1/kappa when kappa is a power of two (then Delta/kappa = Delta * (1/kappa) exactly), else 0
   int reset;          // this step zeroes the stored error
+  float neg_zero;     // -0.0f at run time: addend of the packed products (see device_common.cuh)
 };
 
 struct RankPtrs {

@@ -307,6 +307,15 @@ def test_compress_e8_parity_beta_kappa(L, beta, kappa):
                       70_001, torch.bfloat16, 4, 9)
 
 
+@pytest.mark.parametrize("kappa", [0.5, 1.0, 3.0, 2.0 ** -20, 2.0 ** 20])
+def test_compress_parity_kappa_powers(L, kappa):
+    """kappa a power of two (Delta/kappa taken as an exact product) or not (a division)."""
+    _compress_both(L, dict(bits=8, block=64, beta=0.6, err_scale_mult=kappa, reset_period=0),
+                   20_011, torch.bfloat16, 3, 21)
+    _compress_e8_both(L, dict(bits=4, block=64, beta=0.2, err_scale_mult=kappa, reset_period=0),
+                      20_011, torch.bfloat16, 3, 22)
+
+
 @pytest.mark.parametrize("s", [2.0 ** 19, 2.0 ** 17])
 def test_compress_e8_parity_fixed_scale(L, s):
     _compress_e8_both(L, dict(bits=4, block=128, beta=0.5, err_scale_mult=6.0, reset_period=2),
