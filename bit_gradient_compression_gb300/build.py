@@ -26,8 +26,13 @@ SOURCES = ["abi.cu", "compress.cu", "decode_reduce.cu", "adam.cu", "sgd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere; every fp32 product and sum
 # in the kernels is its own rounded operation, as the method's definition states.
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2",
+# Hidden visibility: only the LOCO_API entry points of include/loco.h are
+# exported; the static CUDA runtime's symbols are kept out of the dynamic
+# symbol table too (--exclude-libs), so nothing can be interposed between this
+# library and other CUDA code in the same process.
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
                      "-I", INCLUDE, "-I", CSRC]
+LINK_FLAGS = ARCH + ["-shared", "-cudart", "static", "-Xlinker", "--exclude-libs,ALL"]
 
 
 def nvcc() -> str:
@@ -74,7 +79,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str =
                     raise RuntimeError(f"nvcc failed on {c[-3]}")
     if force or jobs or _stale(out, objs):
         tmp = out + f".tmp{os.getpid()}"
-        subprocess.check_call([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
+        subprocess.check_call([nvcc(), *LINK_FLAGS, "-o", tmp, *objs])
         os.replace(tmp, out)
     return out
 

@@ -1,7 +1,8 @@
 // Receiver average of Eqn (8) fed to one Adam(W) step (§4 Eqn 9) of "LoCo:
 // Low-Bit Communication Adaptor for Large-scale Model Training": param, m, v,
-// codes and steps staged per tile; the updated param, m, v (and optionally the
-// bf16 copy of param) stored straight from registers.
+// codes and steps staged per tile; the updated param, m, v are written back
+// into their staged slots and leave as three bulk (TMA) stores per tile (full,
+// contiguous lines), the optional bf16 copy of param straight from registers.
 #include "receiver_common.cuh"
 
 namespace loco {
@@ -13,7 +14,10 @@ namespace loco {
 #define LOCO_ADAM_MIN_CTAS 2  // CTAs per SM the stage count is fitted for (measured best)
 #endif
 #ifndef LOCO_ADAM_STAGES
-#define LOCO_ADAM_STAGES 2
+#define LOCO_ADAM_STAGES 3
+#endif
+#ifndef LOCO_ADAM_BULK
+#define LOCO_ADAM_BULK 1  // results written back into the stage and shipped by bulk (TMA) stores (0: direct stores)
 #endif
 
 // One Adam(W) update of one element, in the order the header states.
@@ -29,46 +33,66 @@ __device__ __forceinline__ void adam_elem(const AdamArgs& a, float g, float& p, 
 // Three CTAs per SM is what the two-stage staging allows; the bound keeps every
 // rank count within the matching register budget (one instantiation otherwise
 // took 96 registers and ran at two CTAs per SM).
-template <int BITS, int W, int E, int S, bool BF16OUT>
+template <int BITS, int W, int E, int S, bool BF16OUT, bool BULK>
 __global__ void __launch_bounds__(kThreads, 3) k_adam(const AdamArgs a, int log2_block) {
   using TL = Tile<BITS, W, E, 3>;
   const float* farr[3] = {a.param, a.m, a.v};
-  tile_pipeline<BITS, W, E, 3, S>(
-      farr, a.ranks, a.n, log2_block,
-      [&](const TL& tl, int64_t e0) {
-        const int t = threadIdx.x;
-        float p[E], m[E], v[E], g[E];
+  auto body = [&](const TL& tl, int64_t e0) {
+    const int t = threadIdx.x;
+    float p[E], m[E], v[E], g[E];
 #pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-          const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
-          const float4 mv = reinterpret_cast<const float4*>(tl.f(1) + t * E)[q];
-          const float4 vv = reinterpret_cast<const float4*>(tl.f(2) + t * E)[q];
-          p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
-          m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
-          v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
-        }
-        tile_mean<BITS, W, E, 3>(tl, t, log2_block, a.ranks.neg_zero, g);
+    for (int q = 0; q < E / 4; ++q) {
+      const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
+      const float4 mv = reinterpret_cast<const float4*>(tl.f(1) + t * E)[q];
+      const float4 vv = reinterpret_cast<const float4*>(tl.f(2) + t * E)[q];
+      p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
+      m[4 * q] = mv.x; m[4 * q + 1] = mv.y; m[4 * q + 2] = mv.z; m[4 * q + 3] = mv.w;
+      v[4 * q] = vv.x; v[4 * q + 1] = vv.y; v[4 * q + 2] = vv.z; v[4 * q + 3] = vv.w;
+    }
+    tile_mean<BITS, W, E, 3>(tl, t, log2_block, a.ranks.neg_zero, g);
 #pragma unroll
-        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
-        store_vec<E>(a.param, e0, a.n, true, p);
-        store_vec<E>(a.m, e0, a.n, true, m);
-        store_vec<E>(a.v, e0, a.n, true, v);
-        if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, true, p);
-      },
-      [&](int64_t e0) {
-        const bool full = e0 + E <= a.n;
-        float p[E], m[E], v[E], g[E];
-        load_vec<E>(a.param, e0, a.n, full, p);
-        load_vec<E>(a.m, e0, a.n, full, m);
-        load_vec<E>(a.v, e0, a.n, full, v);
-        decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
+    for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+    if constexpr (BULK) {
+      // results back into the thread's own staged slots; thread 0 ships them
 #pragma unroll
-        for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
-        store_vec<E>(a.param, e0, a.n, full, p);
-        store_vec<E>(a.m, e0, a.n, full, m);
-        store_vec<E>(a.v, e0, a.n, full, v);
-        if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, full, p);
-      });
+      for (int q = 0; q < E / 4; ++q) {
+        reinterpret_cast<float4*>(tl.f(0) + t * E)[q] = make_float4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+        reinterpret_cast<float4*>(tl.f(1) + t * E)[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+        reinterpret_cast<float4*>(tl.f(2) + t * E)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    } else {
+      store_vec<E>(a.param, e0, a.n, true, p);
+      store_vec<E>(a.m, e0, a.n, true, m);
+      store_vec<E>(a.v, e0, a.n, true, v);
+    }
+    if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, true, p);
+  };
+  auto tail = [&](int64_t e0) {
+    const bool full = e0 + E <= a.n;
+    float p[E], m[E], v[E], g[E];
+    load_vec<E>(a.param, e0, a.n, full, p);
+    load_vec<E>(a.m, e0, a.n, full, m);
+    load_vec<E>(a.v, e0, a.n, full, v);
+    decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
+#pragma unroll
+    for (int j = 0; j < E; ++j) adam_elem(a, g[j], p[j], m[j], v[j]);
+    store_vec<E>(a.param, e0, a.n, full, p);
+    store_vec<E>(a.m, e0, a.n, full, m);
+    store_vec<E>(a.v, e0, a.n, full, v);
+    if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, full, p);
+  };
+  if constexpr (BULK) {
+    tile_pipeline_inplace<BITS, W, E, 3, S>(farr, a.ranks, a.n, log2_block, body, tail,
+                                            [&](const TL& tl, int64_t tile) {
+                                              const int64_t off = tile * TL::T;
+                                              bulk_store(a.param + off, tl.f(0), uint32_t(TL::T * 4));
+                                              bulk_store(a.m + off, tl.f(1), uint32_t(TL::T * 4));
+                                              bulk_store(a.v + off, tl.f(2), uint32_t(TL::T * 4));
+                                              bulk_commit();
+                                            });
+  } else {
+    tile_pipeline<BITS, W, E, 3, S>(farr, a.ranks, a.n, log2_block, body, tail);
+  }
 }
 
 template <int BITS, bool BF16OUT>
@@ -80,9 +104,10 @@ struct AdamLaunch {
       constexpr int S = fit_stages<BITS, W, E, 3>(LOCO_ADAM_STAGES, 0, LOCO_ADAM_MIN_CTAS);
       constexpr size_t smem = S * Tile<BITS, W, E, 3>::kBytes;
       static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
-      const void* fn = reinterpret_cast<const void*>(&k_adam<BITS, W, E, S, BF16OUT>);
+      constexpr bool BULK = LOCO_ADAM_BULK != 0 && S >= 2;  // one stage: no room to refill behind a bulk store
+      const void* fn = reinterpret_cast<const void*>(&k_adam<BITS, W, E, S, BF16OUT, BULK>);
       static const int cap = receiver_grid(fn, smem);
-      k_adam<BITS, W, E, S, BF16OUT><<<clamp_grid(a.n, kThreads * E, cap), kThreads, smem, s>>>(a, ilog2_int(a.block));
+      k_adam<BITS, W, E, S, BF16OUT, BULK><<<clamp_grid(a.n, kThreads * E, cap), kThreads, smem, s>>>(a, ilog2_int(a.block));
       return cudaGetLastError();
     }
   };

@@ -115,6 +115,45 @@ __device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, 
   cp_async_wait<0>();
 }
 
+// Variant for kernels that write a tile's results back into its own stage
+// and ship them with bulk (TMA) stores issued by thread 0 (`flush`).  A
+// stage is refilled only after those stores have read it: thread 0 waits for
+// the reads before the barrier that opens each tile, and the refill copies
+// are issued after that barrier.  The tile consumed at step k lives in stage
+// k mod S; the refill at step k goes to the previous tile's stage, S-1 tiles
+// ahead, so S-1 tiles are in flight as in pipeline_tiles.  Hardware waits
+// only, every barrier reached by all threads.
+//   flush(stage_base, tile): (thread 0) bulk stores of the tile's results + commit
+template <int S, typename Issue, typename Body, typename Flush>
+__device__ __forceinline__ void pipeline_tiles_inplace(uint8_t* sm, size_t stage_bytes, int64_t ntiles, Issue issue,
+                                                       Body body, Flush flush) {
+  static_assert(S >= 2, "one stage computes while the next loads");
+  const bool leader = threadIdx.x == 0;
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    const int64_t tile = blockIdx.x + int64_t(s) * gridDim.x;
+    if (tile < ntiles) issue(sm + s * stage_bytes, tile);
+    cp_async_commit();
+  }
+  int cur = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    cp_async_wait<S - 2>();                // this tile's copies have landed
+    if (leader) bulk_wait_read_all();      // the previous tile's results have left its stage
+    __syncthreads();
+    const int prev = (cur == 0) ? S - 1 : cur - 1;
+    const int64_t ahead = tile + int64_t(S - 1) * gridDim.x;
+    if (ahead < ntiles) issue(sm + prev * stage_bytes, ahead);
+    cp_async_commit();
+    body(sm + cur * stage_bytes, tile);
+    fence_smem_to_async_proxy();           // this thread's results visible to the bulk copy
+    __syncthreads();
+    if (leader) flush(sm + cur * stage_bytes, tile);
+    cur = (cur + 1 == S) ? 0 : cur + 1;
+  }
+  cp_async_wait<0>();
+  if (leader) bulk_wait_all();
+}
+
 template <int S, typename Issue, typename Body>
 __device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, int64_t ntiles, Issue issue,
                                                Body body) {

@@ -138,6 +138,27 @@ __device__ __forceinline__ void tile_pipeline(const float* const* farr, const Ra
   }
 }
 
+// Same walk with the results written back into the staged fp32 arrays and
+// shipped by `flush` (see pipeline_tiles_inplace).
+template <int BITS, int W, int E, int NF, int S, typename Body, typename TailFn, typename Flush>
+__device__ __forceinline__ void tile_pipeline_inplace(const float* const* farr, const RankPtrs& rp, int64_t n,
+                                                      int log2_block, Body body, TailFn tail, Flush flush) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  using TL = Tile<BITS, W, E, NF>;
+  const int t = threadIdx.x;
+  const int64_t ntiles = n / TL::T;
+  const int nsc = TL::T >> log2_block;
+  pipeline_tiles_inplace<S>(
+      sm, TL::kBytes, ntiles,
+      [&](uint8_t* st, int64_t tile) { issue_tile<BITS, W, E, NF>(TL{st}, farr, rp, tile, nsc, t); },
+      [&](uint8_t* st, int64_t tile) { body(TL{st}, tile * TL::T + int64_t(t) * E); },
+      [&](uint8_t* st, int64_t tile) { flush(TL{st}, tile); });
+  if (ntiles * TL::T < n && blockIdx.x == ntiles % gridDim.x) {
+    const int64_t e0 = ntiles * TL::T + int64_t(t) * E;
+    if (e0 < n) tail(e0);
+  }
+}
+
 template <int BITS, int W, int E, int NF, int S, typename Body, typename TailFn>
 __device__ __forceinline__ void tile_pipeline(const float* const* farr, const RankPtrs& rp, int64_t n, int log2_block,
                                               Body body, TailFn tail) {

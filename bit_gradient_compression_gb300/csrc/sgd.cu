@@ -1,7 +1,8 @@
 // Receiver average of Eqn (8) fed to one LoCo-SGD step (§4 of "LoCo: Low-Bit
 // Communication Adaptor for Large-scale Model Training": theta = theta -
-// eta * g~): param, codes and steps staged per tile; the updated param (and
-// optionally its bf16 copy) stored straight from registers.
+// eta * g~): param, codes and steps staged per tile; the updated param is
+// written back into its staged slots and leaves as one bulk (TMA) store per
+// tile, the optional bf16 copy straight from registers.
 #include "receiver_common.cuh"
 
 namespace loco {
@@ -15,37 +16,53 @@ namespace loco {
 #ifndef LOCO_SGD_STAGES
 #define LOCO_SGD_STAGES 3
 #endif
+#ifndef LOCO_SGD_BULK
+#define LOCO_SGD_BULK 1  // the updated param written back into the stage and shipped by a bulk (TMA) store (0: direct)
+#endif
 
-template <int BITS, int W, int E, int S, bool BF16OUT>
+template <int BITS, int W, int E, int S, bool BF16OUT, bool BULK>
 __global__ void __launch_bounds__(kThreads) k_sgd(const SgdArgs a, int log2_block) {
   using TL = Tile<BITS, W, E, 1>;
   const float* farr[1] = {a.param};
-  tile_pipeline<BITS, W, E, 1, S>(
-      farr, a.ranks, a.n, log2_block,
-      [&](const TL& tl, int64_t e0) {
-        const int t = threadIdx.x;
-        float p[E], g[E];
+  auto body = [&](const TL& tl, int64_t e0) {
+    const int t = threadIdx.x;
+    float p[E], g[E];
 #pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-          const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
-          p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
-        }
-        tile_mean<BITS, W, E, 1>(tl, t, log2_block, a.ranks.neg_zero, g);
+    for (int q = 0; q < E / 4; ++q) {
+      const float4 pv = reinterpret_cast<const float4*>(tl.f(0) + t * E)[q];
+      p[4 * q] = pv.x; p[4 * q + 1] = pv.y; p[4 * q + 2] = pv.z; p[4 * q + 3] = pv.w;
+    }
+    tile_mean<BITS, W, E, 1>(tl, t, log2_block, a.ranks.neg_zero, g);
 #pragma unroll
-        for (int j = 0; j < E; ++j) p[j] = __fsub_rn(p[j], __fmul_rn(a.lr, g[j]));
-        store_vec<E>(a.param, e0, a.n, true, p);
-        if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, true, p);
-      },
-      [&](int64_t e0) {
-        const bool full = e0 + E <= a.n;
-        float p[E], g[E];
-        load_vec<E>(a.param, e0, a.n, full, p);
-        decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
+    for (int j = 0; j < E; ++j) p[j] = __fsub_rn(p[j], __fmul_rn(a.lr, g[j]));
+    if constexpr (BULK) {
 #pragma unroll
-        for (int j = 0; j < E; ++j) p[j] = __fsub_rn(p[j], __fmul_rn(a.lr, g[j]));
-        store_vec<E>(a.param, e0, a.n, full, p);
-        if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, full, p);
-      });
+      for (int q = 0; q < E / 4; ++q)
+        reinterpret_cast<float4*>(tl.f(0) + t * E)[q] = make_float4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+    } else {
+      store_vec<E>(a.param, e0, a.n, true, p);
+    }
+    if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, true, p);
+  };
+  auto tail = [&](int64_t e0) {
+    const bool full = e0 + E <= a.n;
+    float p[E], g[E];
+    load_vec<E>(a.param, e0, a.n, full, p);
+    decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, g);
+#pragma unroll
+    for (int j = 0; j < E; ++j) p[j] = __fsub_rn(p[j], __fmul_rn(a.lr, g[j]));
+    store_vec<E>(a.param, e0, a.n, full, p);
+    if constexpr (BF16OUT) store_bf16<E>(a.param_bf16, e0, a.n, full, p);
+  };
+  if constexpr (BULK) {
+    tile_pipeline_inplace<BITS, W, E, 1, S>(farr, a.ranks, a.n, log2_block, body, tail,
+                                            [&](const TL& tl, int64_t tile) {
+                                              bulk_store(a.param + tile * TL::T, tl.f(0), uint32_t(TL::T * 4));
+                                              bulk_commit();
+                                            });
+  } else {
+    tile_pipeline<BITS, W, E, 1, S>(farr, a.ranks, a.n, log2_block, body, tail);
+  }
 }
 
 template <int BITS, bool BF16OUT>
@@ -57,9 +74,10 @@ struct SgdLaunch {
       constexpr int S = fit_stages<BITS, W, E, 1>(LOCO_SGD_STAGES, 0, LOCO_SGD_MIN_CTAS);
       constexpr size_t smem = S * Tile<BITS, W, E, 1>::kBytes;
       static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
-      const void* fn = reinterpret_cast<const void*>(&k_sgd<BITS, W, E, S, BF16OUT>);
+      constexpr bool BULK = LOCO_SGD_BULK != 0 && S >= 2;  // one stage: no room to refill behind a bulk store
+      const void* fn = reinterpret_cast<const void*>(&k_sgd<BITS, W, E, S, BF16OUT, BULK>);
       static const int cap = receiver_grid(fn, smem);
-      k_sgd<BITS, W, E, S, BF16OUT><<<clamp_grid(a.n, kThreads * E, cap), kThreads, smem, s>>>(a, ilog2_int(a.block));
+      k_sgd<BITS, W, E, S, BF16OUT, BULK><<<clamp_grid(a.n, kThreads * E, cap), kThreads, smem, s>>>(a, ilog2_int(a.block));
       return cudaGetLastError();
     }
   };

@@ -42,6 +42,16 @@
 #include <stdint.h>
 #include <stddef.h>
 
+/* The entry points below are the only symbols the library exports; every
+ * other symbol (kernels, helpers, the statically linked CUDA runtime) is
+ * hidden, so the library can share a process with other CUDA code, including
+ * another build of itself. */
+#if defined(__GNUC__) || defined(__clang__)
+#define LOCO_API __attribute__((visibility("default")))
+#else
+#define LOCO_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -90,10 +100,10 @@ typedef struct {
 } loco_adam_hparams;
 
 /* nb = ceil(n / block); 0 for n <= 0 or block <= 0. */
-int64_t loco_num_blocks(int64_t n, int32_t block);
+LOCO_API int64_t loco_num_blocks(int64_t n, int32_t block);
 
 /* Bytes of packed codes for a bucket of n elements: nb * block * bits / 8; 0 on bad arguments. */
-int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block);
+LOCO_API int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block);
 
 /*
  * loco_compress — sender side of one LoCo step on one rank's flat gradient bucket.
@@ -123,7 +133,7 @@ int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block);
  * n == 0 is a valid empty call: nothing is launched.
  * grad must not alias err, codes or scales.
  */
-loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad_dtype,
+LOCO_API loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad_dtype,
                           float* err, int64_t n, int64_t step,
                           uint8_t* codes, float* scales, loco_stream_t stream);
 
@@ -146,7 +156,7 @@ loco_status loco_compress(const loco_config* cfg, const void* grad, int32_t grad
  * Delta/(2*kappa) to be stored at all, so beta (weight of the previous error)
  * should be well below 1 with this storage.
  */
-loco_status loco_compress_e8(const loco_config* cfg, const void* grad, int32_t grad_dtype,
+LOCO_API loco_status loco_compress_e8(const loco_config* cfg, const void* grad, int32_t grad_dtype,
                              int8_t* err_codes, float* err_steps, int64_t n, int64_t step,
                              uint8_t* codes, float* scales, loco_stream_t stream);
 
@@ -163,7 +173,7 @@ loco_status loco_compress_e8(const loco_config* cfg, const void* grad, int32_t g
  * are read.  mean [n] device fp32, out; it must not alias any input.
  * 1 <= W <= LOCO_MAX_RANKS.
  */
-loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* codes,
+LOCO_API loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* codes,
                                const float* const* scales, int32_t W, int64_t n,
                                float* mean, loco_stream_t stream);
 
@@ -187,7 +197,7 @@ loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* cod
  * beta2 = 1-beta2_paper, bias_correction = 0, eps_inside_sqrt = 1.
  * param, m, v [n] device fp32, in/out.  t = 1-based optimizer step.
  */
-loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes,
+LOCO_API loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes,
                            const float* const* scales, int32_t W, int64_t n,
                            float* param, float* m, float* v,
                            const loco_adam_hparams* hp, int64_t t, loco_stream_t stream);
@@ -199,7 +209,7 @@ loco_status loco_adam_step(const loco_config* cfg, const uint8_t* const* codes,
  * all-gathers after the update (the 16-bit parameters of the Table I memory
  * and communication comparison, §4).  Everything else as loco_adam_step.
  */
-loco_status loco_adam_step_bf16(const loco_config* cfg, const uint8_t* const* codes,
+LOCO_API loco_status loco_adam_step_bf16(const loco_config* cfg, const uint8_t* const* codes,
                                 const float* const* scales, int32_t W, int64_t n,
                                 float* param, float* m, float* v, uint16_t* param_bf16,
                                 const loco_adam_hparams* hp, int64_t t, loco_stream_t stream);
@@ -212,16 +222,16 @@ loco_status loco_adam_step_bf16(const loco_config* cfg, const uint8_t* const* co
  * param [n] device fp32, in/out.  param_bf16 [n] device, out, or NULL: when
  * given it receives the updated parameters rounded to bf16 (nearest even).
  */
-loco_status loco_sgd_step(const loco_config* cfg, const uint8_t* const* codes,
+LOCO_API loco_status loco_sgd_step(const loco_config* cfg, const uint8_t* const* codes,
                           const float* const* scales, int32_t W, int64_t n,
                           float* param, uint16_t* param_bf16, float lr, loco_stream_t stream);
 
 /* Static text for a status code. */
-const char* loco_status_string(loco_status s);
+LOCO_API const char* loco_status_string(loco_status s);
 
 /* Text of the last LOCO_ERR_CUDA (or argument error) raised on the calling
  * host thread; "" if none.  Thread local; valid until the next call. */
-const char* loco_last_error(void);
+LOCO_API const char* loco_last_error(void);
 
 #ifdef __cplusplus
 }

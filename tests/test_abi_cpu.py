@@ -32,6 +32,36 @@ def test_exports_every_declared_symbol(L):
     assert set(names) == set(L.EXPORTS)
 
 
+def _defined_dynamic_symbols(path):
+    """Names of the global/weak symbols an ELF64 little-endian shared object defines (.dynsym)."""
+    import struct
+    data = open(path, "rb").read()
+    assert data[:4] == b"\x7fELF" and data[4] == 2 and data[5] == 1, "ELF64 little-endian expected"
+    shoff, = struct.unpack_from("<Q", data, 0x28)
+    shentsize, shnum = struct.unpack_from("<HH", data, 0x3A)
+    secs = [struct.unpack_from("<IIQQQQIIQQ", data, shoff + i * shentsize) for i in range(shnum)]
+    names = set()
+    for sec in secs:
+        if sec[1] != 11:  # SHT_DYNSYM
+            continue
+        strtab = secs[sec[6]]
+        off, size, entsize = sec[4], sec[5], sec[9]
+        for k in range(1, size // entsize):
+            st_name, st_info, _, st_shndx, _, _ = struct.unpack_from("<IBBHQQ", data, off + k * entsize)
+            if st_shndx == 0 or (st_info >> 4) not in (1, 2):  # undefined, or not GLOBAL/WEAK
+                continue
+            s0 = strtab[4] + st_name
+            names.add(data[s0:data.index(b"\0", s0)].decode())
+    return names
+
+
+def test_exports_nothing_else(L):
+    """Only the header's entry points are visible: kernels, helpers and the
+    static CUDA runtime stay hidden, so nothing can be interposed between the
+    library and other CUDA code (or another build of itself) in one process."""
+    assert _defined_dynamic_symbols(L.LIB_PATH) == set(header_functions())
+
+
 def test_sizes(L):
     assert L.loco_num_blocks(0, 256) == 0
     assert L.loco_num_blocks(1, 256) == 1
