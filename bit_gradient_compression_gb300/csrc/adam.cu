@@ -20,14 +20,33 @@ namespace loco {
 #define LOCO_ADAM_BULK 1  // results written back into the stage and shipped by bulk (TMA) stores (0: direct stores)
 #endif
 
+// IEEE square root and quotient with a zero operand handled by a select: the
+// operation is evaluated on 1 instead and the exact IEEE result put back
+// (sqrt(+-0) = +-0; +-0 / d = +-0 for a finite d > 0), so an element whose
+// mean gradient has been exactly zero (m = v = 0) does not send its warp down
+// the special-value path of the rounded square root or division.  The results
+// are those of __fsqrt_rn / __fdiv_rn for every input.  Measured: with 2.5 %
+// of the means exactly zero (two ranks' 4-bit codes of Gaussian gradients) the
+// step ran at 71 % of the HBM copy rate without the selects and 97 % with them.
+__device__ __forceinline__ float sqrt_zsel(float x) {
+  const bool z = x == 0.0f;
+  const float r = __fsqrt_rn(z ? 1.0f : x);
+  return z ? x : r;
+}
+__device__ __forceinline__ float div_zsel(float n, float d) {
+  const bool z = n == 0.0f && d > 0.0f && d < INFINITY;
+  const float r = __fdiv_rn(z ? 1.0f : n, d);
+  return z ? n : r;
+}
+
 // One Adam(W) update of one element, in the order the header states.
 __device__ __forceinline__ void adam_elem(const AdamArgs& a, float g, float& p, float& m, float& v) {
   p = __fsub_rn(p, __fmul_rn(a.lr_wd, p));
   m = __fadd_rn(__fmul_rn(a.beta1, m), __fmul_rn(a.one_minus_beta1, g));
   v = __fadd_rn(__fmul_rn(a.beta2, v), __fmul_rn(a.one_minus_beta2, __fmul_rn(g, g)));
-  const float den = a.eps_inside_sqrt ? __fsqrt_rn(__fadd_rn(__fmul_rn(v, a.c2), a.eps))
-                                      : __fadd_rn(__fmul_rn(__fsqrt_rn(v), a.c2), a.eps);
-  p = __fsub_rn(p, __fmul_rn(a.c1, __fdiv_rn(m, den)));
+  const float den = a.eps_inside_sqrt ? sqrt_zsel(__fadd_rn(__fmul_rn(v, a.c2), a.eps))
+                                      : __fadd_rn(__fmul_rn(sqrt_zsel(v), a.c2), a.eps);
+  p = __fsub_rn(p, __fmul_rn(a.c1, div_zsel(m, den)));
 }
 
 // Three CTAs per SM is what the two-stage staging allows; the bound keeps every

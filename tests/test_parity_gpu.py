@@ -200,6 +200,44 @@ def test_adam_parity(L, W, bits, block, variant):
             assert_bits_equal(v.cpu().numpy(), vh, f"v n={n} t={t}")
 
 
+@pytest.mark.parametrize("eps_inside_sqrt", [False, True])
+@pytest.mark.parametrize("W", [1, 2, 5])
+def test_adam_parity_zero_and_underflowing_means(L, W, eps_inside_sqrt):
+    """Means that are exactly zero (every rank's codes 0 in a block, so m = v = 0
+    and the step takes sqrt(0) and 0 / den) and means so small that g*g
+    underflows (v = 0 while m != 0), mixed with ordinary blocks, over several
+    steps and at sizes that span many tiles plus a ragged tail."""
+    bits, block = 4, 64
+    cfg = L.make_config(bits=bits, block=block)
+    hpk = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8 if not eps_inside_sqrt else 1e-16, weight_decay=0.0,
+               bias_correction=True, eps_inside_sqrt=eps_inside_sqrt)
+    hp = L.make_adam(**hpk)
+    n = 3 * 2048 * 8 + 77
+    nb = L.loco_num_blocks(n, block)
+    kind = np.arange(nb) % 5            # 0, 1: zero codes; 2: tiny steps; 3, 4: ordinary
+    p = wl().fill_uniform(torch.empty(n, device=DEV), 3, -0.05, 0.05)
+    m = torch.zeros(n, device=DEV)
+    v = torch.zeros(n, device=DEV)
+    ph, mh, vh = p.cpu().numpy().copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    for t in (1, 2, 3):
+        codes, scales = _random_ranks(L, n, bits, block, W, 40 + t)
+        for w in range(W):
+            c = codes[w].cpu().numpy().reshape(nb, block * bits // 8)
+            c[kind <= 1] = 0
+            codes[w].copy_(torch.from_numpy(c.reshape(-1)))
+            sc = scales[w].cpu().numpy()
+            sc[kind == 2] = np.float32(1e-24)
+            scales[w].copy_(torch.from_numpy(sc))
+        L.loco_adam_step(cfg, codes, scales, n, p, m, v, hp, t)
+        oracle.adam_step([c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales], n, ph, mh, vh,
+                         t, bits=bits, block=block, **hpk)
+        torch.cuda.synchronize()
+        assert_bits_equal(p.cpu().numpy(), ph, f"param t={t}")
+        assert_bits_equal(m.cpu().numpy(), mh, f"m t={t}")
+        assert_bits_equal(v.cpu().numpy(), vh, f"v t={t}")
+    assert ((vh == 0) & (mh == 0)).any() and ((vh == 0) & (mh != 0)).any(), "edge cases not reached"
+
+
 def test_flat_1m_config_full(L):
     """The 1M-element fp32 workload: 4 ranks, 8 steps, 4-bit, block 256,
     beta 0.9 -- every rank's codes, scales and error, and the mean, compared in
