@@ -38,22 +38,17 @@ __device__ __forceinline__ void st_stream(uint2* p, uint2 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint32_t* p, uint32_t v) { __stcs(p, v); }
 
 // ---------------------------------------------------------------------------
-// Asynchronous global -> shared copies (cp.async).  Each thread copies the
-// bytes it will itself consume and waits with cp.async.wait_group, so the
-// staging needs neither block barriers nor spin-waits; the bytes in flight
-// live in shared memory instead of registers.
+// Asynchronous global -> shared copies (cp.async, 16 bytes per instruction).
+// Completion is tracked per thread by commit groups and waited for with the
+// hardware cp.async.wait_group; a block barrier then makes every thread's
+// copies visible to the others (see pipeline_tiles).  The bytes in flight live
+// in shared memory instead of registers, and no thread spins on a flag.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -236,15 +231,6 @@ struct ChunkCodes {
       w[0] = v.x;
       w[1] = v.y;
     }
-  }
-
-  // Start an asynchronous copy of this chunk's codes into shared memory.
-  __device__ __forceinline__ static void prefetch(uint8_t* dst, const uint8_t* base, int64_t e0) {
-    const uint8_t* p = base + (e0 * BITS >> 3);
-    if constexpr (kWords == 1)
-      cp_async4(dst, p);
-    else
-      cp_async8(dst, p);
   }
 
   __device__ __forceinline__ void load_shared(const uint8_t* src) {
