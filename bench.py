@@ -376,12 +376,15 @@ def run_e2e(args, L, w, cfg, n, nb, cb, g, compress, update, codes, scales, mean
     for dst_, src_ in ((dst, src), (src, dst)):
         dst_.copy_(src_, non_blocking=True)
         torch.cuda.synchronize()
-        a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(comp)
-        dst_.copy_(src_, non_blocking=True)
-        b0.record(comp)
-        torch.cuda.synchronize()
-        link.append(probe_n / (a0.elapsed_time(b0) * 1e-3) / 1e9)
+        best = 0.0
+        for _ in range(3):  # a single copy can be far slower than the link sustains: keep the best of three
+            a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(comp)
+            dst_.copy_(src_, non_blocking=True)
+            b0.record(comp)
+            torch.cuda.synchronize()
+            best = max(best, probe_n / (a0.elapsed_time(b0) * 1e-3) / 1e9)
+        link.append(best)
     g.copy_(g_h)
     torch.cuda.synchronize()
     K = args.e2e_steps
@@ -607,6 +610,7 @@ def run_loco(args, rank, world):
                       "steps": args.e2e_steps,
                       "host_link_GBps": {"h2d": round(link[0], 1), "d2h": round(link[1], 1)},
                       "copy_bound_ms_per_step": round(h2d / (link[0] * 1e9) * 1e3, 1),
+                      "achieved_h2d_GBps": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
                       "what": "page-locked host -> device: rank 0 gradient + ranks 1..W-1 packed buffers; "
                               "device -> page-locked host: rank 0's packed buffer; copies on their own streams "
                               "overlap the previous step's kernels (double-buffered device inputs)"}
