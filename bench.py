@@ -103,7 +103,8 @@ def kernel_bytes(n, gsize, bits, block, W, e8=False, optimizer="adam", bf16_out=
     sb = nb * 4
     opt_state = 24 if optimizer == "adam" else 8   # param (+ m, v) read and written
     return {
-        "compress": n * gsize + (2 * n + 3 * sb if e8 else 8 * n) + cb + sb,
+        # int8 error: codes read + written (2 B) and the block step read + written; fp32: 4 B read + 4 B written
+        "compress": n * gsize + (2 * n + 2 * sb if e8 else 8 * n) + cb + sb,
         "decode_reduce": W * (cb + sb) + 4 * n,
         optimizer: W * (cb + sb) + opt_state * n + (2 * n if bf16_out else 0),
     }

@@ -59,3 +59,35 @@ def test_workload_overrides():
     assert (o.n, o.bits, o.block, o.W) == (1 << 30, 8, 256, 16)
     assert o.name == "flat-bf16-2^30[bits=8,W=16]"                # a changed config never matches stored counters
     assert bench.kernel_bytes(1 << 10, 2, 8, 256, 16)["decode_reduce"] == 16 * (1024 + 16) + 4096
+
+
+def test_algorithmic_bytes_per_element():
+    """The roofline numerators: bytes per element of each kernel as the method
+    moves them (gradient read, fp32 error read and written, p/8 code bytes and a
+    4-byte step per block written; W ranks' codes and steps read by a receiver,
+    the fp32 mean written, or param/m/v read and written)."""
+    import bench
+    n = 1 << 20
+    per = lambda d: {k: v / n for k, v in d.items()}
+    b = per(bench.kernel_bytes(n, 2, 4, 256, 8))                 # bf16 gradient, 4-bit, block 256, W 8
+    assert b["compress"] == pytest.approx(10.515625)
+    assert b["decode_reduce"] == pytest.approx(8.125)
+    assert b["adam"] == pytest.approx(28.125)
+    assert per(bench.kernel_bytes(n, 4, 4, 256, 8))["compress"] == pytest.approx(12.515625)   # fp32 gradient
+    assert per(bench.kernel_bytes(n, 2, 8, 128, 8))["compress"] == pytest.approx(11.03125)    # 8-bit, block 128
+    e8 = per(bench.kernel_bytes(n, 2, 4, 256, 8, e8=True))      # int8 error: 1 B read + 1 B written + 2 steps/block
+    assert e8["compress"] == pytest.approx(2 + 1 + 1 + 0.5 + 12 / 256)
+    sgd = per(bench.kernel_bytes(n, 2, 4, 256, 8, optimizer="sgd", bf16_out=True))
+    assert sgd["sgd"] == pytest.approx(8 * (0.5 + 4 / 256) + 8 + 2)
+    # gradient-equivalent units behind the headline value
+    u = bench.grad_units(n, 2, 8)
+    assert u == {"compress": 2 * n, "decode_reduce": 16 * n, "adam": 16 * n}
+
+
+def test_workload_sizes():
+    """Parameter counts of the model-shaped buckets, summed from their layouts."""
+    import bench
+    assert bench.workload("llama2-7b").n == 6_738_415_616
+    assert bench.workload("tinyllama").n == 1_100_048_384
+    assert bench.workload("mixtral").n == 8 * 3 * 14336 * 4096
+    assert bench.workload("flat:26").n == 1 << 26
