@@ -31,8 +31,9 @@
  *    launch: a graph captured at step k replays step k.  The first call of each
  *    configuration (bits, block, W, dtype, ...) queries occupancy and sets the
  *    kernel's shared-memory limit once; make it before capturing.
- *  - Arithmetic is IEEE binary32, round to nearest even, no fused
- *    multiply-add; the exact operation order of each step is stated at the
+ *  - Arithmetic is IEEE binary32, round to nearest even, every product and
+ *    every sum rounded on its own (no product is fused into a following add);
+ *    the exact operation order of each step is stated at the
  *    entry point.  Non-finite inputs are outside the contract: no call reads
  *    or writes out of bounds on them, but the values produced are unspecified.
  */
