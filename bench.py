@@ -336,6 +336,18 @@ def max_over_ranks(values, device):
     return [float(x) for x in t.tolist()]
 
 
+def all_ranks_agree(ok: bool, device) -> bool:
+    """True only if `ok` holds on every rank (a no-op on one rank), so that a
+    leg with collectives inside is entered by all ranks or by none."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return bool(ok)
+    t = torch.tensor([1 if ok else 0], dtype=torch.int32, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(t.item())
+
+
 def whole_job_value(units_per_rank_step: int, world: int, ms_per_step_max: float) -> float:
     """Units every rank processed in one step, over the slowest rank's step time (GB/s)."""
     return world * units_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
@@ -559,15 +571,19 @@ def run_loco(args, rank, world):
     d2h = cb + 4 * nb
     need = h2d + d2h
     avail = host_mem_available()
+    local_ranks = max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))  # ranks sharing this host's memory
     e2e_skip = None
     if args.e2e_steps <= 0:
         e2e_skip = "disabled"
-    elif avail is not None and need > 0.6 * avail:
-        e2e_skip = f"host buffers need {need / 1e9:.1f} GB, only {avail / 1e9:.1f} GB available"
+    elif avail is not None and need > 0.6 * avail / local_ranks:
+        e2e_skip = (f"host buffers need {need / 1e9:.1f} GB per rank, {avail / 1e9:.1f} GB available "
+                    f"for {local_ranks} rank(s)")
     else:
         free_dev = torch.cuda.mem_get_info(dev)[0]
         if h2d + d2h > 0.9 * free_dev:
             e2e_skip = f"second device buffer set needs {(h2d + d2h) / 1e9:.1f} GB, {free_dev / 1e9:.1f} GB free"
+    if not all_ranks_agree(e2e_skip is None, dev) and e2e_skip is None:
+        e2e_skip = "skipped on another rank"
     if e2e_skip is None:
         e2e = run_e2e(args, L, w, cfg, n, nb, cb, g, compress, update, codes, scales, mean, world, dist, h2d, d2h)
 

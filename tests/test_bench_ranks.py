@@ -23,7 +23,8 @@ def _worker(rank, world, port, q):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
     got = bench.max_over_ranks([10.0 + rank, 50.0 - 20.0 * rank], "cpu")
-    q.put((rank, got, bench.whole_job_value(10 ** 9, world, got[0])))
+    agree = (bench.all_ranks_agree(True, "cpu"), bench.all_ranks_agree(rank == 0, "cpu"))
+    q.put((rank, got, bench.whole_job_value(10 ** 9, world, got[0]), agree))
     dist.barrier()
     dist.destroy_process_group()
 
@@ -39,14 +40,16 @@ def test_max_over_ranks_and_value_gloo():
     for p in ps:
         p.join(timeout=60)
         assert p.exitcode == 0
-    for rank, got, value in res:
+    for rank, got, value, agree in res:
         assert got == [11.0, 50.0]
         assert value == pytest.approx(2 * 1e9 / 11e-3 / 1e9)
+        assert agree == (True, False)      # one rank's "no" is every rank's "no"
 
 
 def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks([3.0, 4.0], "cpu") == [3.0, 4.0]
+    assert bench.all_ranks_agree(True, "cpu") is True and bench.all_ranks_agree(False, "cpu") is False
     assert bench.whole_job_value(2 * 10 ** 9, 1, 1000.0) == pytest.approx(2.0)
 
 
