@@ -127,3 +127,50 @@ def test_e8_zero_reset_resume():
         c, s = oracle.compress_e8(gs[k - 1], qe2, de2, k, **kw)
         assert np.array_equal(c, full[k - 1][0]) and np.array_equal(s, full[k - 1][1])
     assert np.array_equal(qe2, qe) and np.array_equal(de2, de)
+
+
+@pytest.mark.parametrize("e8", [False, True])
+@pytest.mark.parametrize("bits,block", [(4, 64), (8, 128)])
+def test_blocks_are_independent_over_steps(e8, bits, block):
+    """Every quant block is its own problem (§3.1: the scale, the codes and the
+    error of a block depend on that block's elements only).  A bucket of several
+    blocks with very different magnitudes, compressed over 5 steps, gives exactly
+    what compressing each block as a bucket of its own gives -- codes, steps and
+    the stored error -- including a ragged last block.  Any read of a neighbouring
+    block's state (scale, error step, error) breaks it."""
+    nblk = 5
+    n = nblk * block - 7
+    rng = np.random.default_rng(11 + bits + block + int(e8))
+    mags = np.float32(10.0) ** np.arange(-4, 1, dtype=np.float32)       # one magnitude per block
+    kw = dict(bits=bits, block=block, beta=0.3, kappa=4.0, reset_period=0)
+    grads = [(rng.standard_normal(n).astype(np.float32) * np.repeat(mags, block)[:n]) for _ in range(5)]
+
+    def run(lo, hi):
+        m = hi - lo
+        if e8:
+            qe, de = _e8_state(m, block)
+        else:
+            err = np.zeros(m, dtype=np.float32)
+        out = []
+        for k, g in enumerate(grads, start=1):
+            if e8:
+                c, s = oracle.compress_e8(np.ascontiguousarray(g[lo:hi]), qe, de, k, **kw)
+                out.append((c.copy(), s.copy(), qe.copy(), de.copy()))
+            else:
+                c, s = oracle.compress(np.ascontiguousarray(g[lo:hi]), err, k, **kw)
+                out.append((c.copy(), s.copy(), err.copy()))
+        return out
+
+    whole = run(0, n)
+    cb = block * bits // 8
+    for b in range(nblk):
+        lo, hi = b * block, min(n, (b + 1) * block)
+        alone = run(lo, hi)
+        for k in range(len(grads)):
+            assert whole[k][0][b * cb:(b + 1) * cb].tobytes() == alone[k][0].tobytes(), ("codes", b, k)
+            assert whole[k][1][b].view(np.uint32) == alone[k][1][0].view(np.uint32), ("step", b, k)
+            if e8:
+                assert np.array_equal(whole[k][2][lo:hi], alone[k][2]), ("error codes", b, k)
+                assert whole[k][3][b].view(np.uint32) == alone[k][3][0].view(np.uint32), ("error step", b, k)
+            else:
+                assert np.array_equal(whole[k][2][lo:hi].view(np.uint32), alone[k][2].view(np.uint32)), ("error", b, k)

@@ -36,6 +36,15 @@ MUTATIONS = [
     ("8-bit error not decompressed", "prev[j] = (float)err_codes[lo + j] * de_prev;", "prev[j] = (float)err_codes[lo + j];", 0),
     ("bf16 truncation instead of rounding", "u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;", 0),
     ("SGD step sign flipped", "float p = param[i] - step;", "float p = param[i] + step;", 0),
+    ("Adam eps dropped (eps outside the root)", "den = rs + eps;", "den = rs;", 0),
+    ("decoupled weight decay dropped", "p = p - decay;", "p = p - 0.0f * decay;", 0),
+    ("clip upper bound 128 codes", "const float e_hi = 127.0f * delta_e;", "const float e_hi = 128.0f * delta_e;", 0),
+    ("padding codes nonzero", "put_code(blk, bits, j, 0);", "put_code(blk, bits, j, 1);", 0),
+    ("int8 error decoded with a neighbouring block's step", "const float de_prev = err_steps[b];",
+     "const float de_prev = err_steps[b > b0 ? b - 1 : b];", 0),
+    ("every rank decoded with rank 0's step", "float d = (float)q * scales[w][b];", "float d = (float)q * scales[0][b];", 0),
+    ("v accumulates |g| instead of g*g", "float gg = g * g;", "float gg = g < 0 ? -g : g;", 0),
+    ("fixed step s instead of 1/s", "delta = 1.0f / fixed_scale;", "delta = fixed_scale;", 0),
 ]
 
 
