@@ -45,6 +45,20 @@ MUTATIONS = [
     ("every rank decoded with rank 0's step", "float d = (float)q * scales[w][b];", "float d = (float)q * scales[0][b];", 0),
     ("v accumulates |g| instead of g*g", "float gg = g * g;", "float gg = g < 0 ? -g : g;", 0),
     ("fixed step s instead of 1/s", "delta = 1.0f / fixed_scale;", "delta = fixed_scale;", 0),
+    ("rank sum in reverse order",
+     "int q = get_code(codes[w] + b * bytes_per_block, bits, j);\n      float d = (float)q * scales[w][b];\n      acc = (w == 0) ? d : acc + d;\n      acc64 += (double)d;",
+     "int q = get_code(codes[W - 1 - w] + b * bytes_per_block, bits, j);\n      float d = (float)q * scales[W - 1 - w][b];\n      acc = (w == 0) ? d : acc + d;\n      acc64 += (double)d;", 0),
+    ("mean divided per term", "acc = (w == 0) ? d : acc + d;\n      acc64 += (double)d;\n    }\n    mean[i] = acc / (float)W;",
+     "acc = (w == 0) ? d / (float)W : acc + d / (float)W;\n      acc64 += (double)d;\n    }\n    mean[i] = acc;", 0),
+    ("Adam m bias correction uses beta2", "c1 = (float)((double)lr / bc1);", "c1 = (float)((double)lr / bc2);", 0),
+    ("inverse step as 1/delta", "inv = (amax == 0.0f) ? 0.0f : qmax / amax;",
+     "inv = (amax == 0.0f) ? 0.0f : 1.0f / (amax / qmax);", 0),
+    ("int8 error inverse as 1/(delta/kappa)", "float inv_e = kappa * inv;",
+     "float inv_e = (de_new == 0.0f) ? 0.0f : 1.0f / de_new;", 0),
+    ("bf16 ties rounded up", "u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;", 0),
+    ("absmax skips the last element", "float amax = 0.0f;\n      for (int64_t j = 0; j < cnt; ++j) {",
+     "float amax = 0.0f;\n      for (int64_t j = 0; j < cnt - 1; ++j) {", 0),
+    ("m accumulates g*g", "float mg = omb1 * g;", "float mg = omb1 * (g * g);", 0),
 ]
 
 

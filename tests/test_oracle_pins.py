@@ -534,3 +534,145 @@ def test_sgd_step_closed_form():
     # decode_reduce gives the same g~
     g = oracle.decode_reduce([codes], [scales], n, bits=bits, block=block)
     assert np.array_equal(p, (p0 - np.float32(2.0 ** -3) * g).astype(np.float32))
+
+
+# ------------------------------------------- rounding paths the readings fix (targeted)
+
+def _rint_even(fr: Fraction) -> int:
+    """Nearest integer to an exact rational, halves to even."""
+    f = fr.numerator // fr.denominator
+    rem = fr - f
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and f % 2 == 1):
+        f += 1
+    return f
+
+
+def _F(x) -> Fraction:
+    return Fraction(float(np.float32(x)))
+
+
+def _inverse_split_case(qmax: int, seed: int):
+    """A block maximum A for which RN(qmax/A) and RN(1/RN(A/qmax)) differ, and an
+    element h of that block whose code differs between the two (exact rationals)."""
+    rng = np.random.default_rng(seed)
+    for A in rng.uniform(0.25, 1.0, 4000).astype(np.float32):
+        inv = f32_nearest(Fraction(qmax) / _F(A))
+        inv_alt = f32_nearest(1 / _F(f32_nearest(_F(A) / qmax)))
+        if inv == inv_alt:
+            continue
+        for k in range(qmax):
+            h0 = np.float32(float((Fraction(k) + Fraction(1, 2)) / _F(inv)))
+            for d in range(-40, 41):
+                h = np.float32(h0)
+                h = np.nextafter(h, np.float32(np.inf) if d > 0 else np.float32(-np.inf)) if d else h
+                for _ in range(abs(d) - 1):
+                    h = np.nextafter(h, np.float32(np.inf) if d > 0 else np.float32(-np.inf))
+                if not (0 < h < A):
+                    continue
+                qa = _rint_even(_F(f32_nearest(_F(h) * _F(inv))))
+                qb = _rint_even(_F(f32_nearest(_F(h) * _F(inv_alt))))
+                if qa != qb:
+                    return A, h, inv, qa, qb
+    raise AssertionError("no distinguishing case found")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_inverse_step_is_rounded_qmax_over_amax(bits):
+    """Reading of Eqn (1): codes are rint(h * inv_b) with inv_b = RN(qmax / A_b),
+    the IEEE quotient -- not the reciprocal of the stored step.  The case is
+    built so that the two inverses round differently and an element's code
+    depends on which one is used."""
+    qmax = (1 << (bits - 1)) - 1
+    A, h, inv, qa, qb = _inverse_split_case(qmax, 40 + bits)
+    block = 64
+    g = np.zeros(block, dtype=np.float32)
+    g[0], g[1] = A, h
+    codes, scales = run(g, np.zeros(block, np.float32), 1, bits=bits, block=block, beta=0.5, kappa=4.0)
+    q = unpack_codes(codes, bits, block)
+    assert scales[0] == f32_nearest(_F(A) / qmax)
+    assert q[0] == qmax and q[1] == qa and qa != qb
+
+
+def test_error_code_inverse_is_kappa_times_inverse_step():
+    """Reading of Eqn (7): the 8-bit error code is rint(t * inv_e) with
+    inv_e = RN(kappa * inv_b) (s_e = kappa * s), not RN(1 / (Delta_b / kappa)).
+    With beta = 0 the stored error before coding is t = r = h - RN(q * Delta_b).
+    The element h is placed so that r * inv_e sits at a half-integer k + 1/2
+    (k <= 2 keeps |r * inv_b| < 1/2, so q is unchanged) and the two inverses give
+    different error codes."""
+    kappa = np.float32(6.0)
+    qmax, block = 7, 64
+    rng = np.random.default_rng(3)
+
+    def nudge(x, steps):
+        for _ in range(abs(steps)):
+            x = np.nextafter(x, np.float32(np.inf) if steps > 0 else np.float32(-np.inf))
+        return x
+
+    found = None
+    for A in rng.uniform(0.25, 1.0, 3000).astype(np.float32):
+        inv = f32_nearest(Fraction(qmax) / _F(A))
+        delta = f32_nearest(_F(A) / qmax)
+        inv_e = f32_nearest(_F(kappa) * _F(inv))
+        inv_e_alt = f32_nearest(1 / _F(f32_nearest(_F(delta) / _F(kappa))))
+        if inv_e == inv_e_alt:
+            continue
+        for q in (1, 2, 3):
+            d = f32_nearest(q * _F(delta))
+            for k in (0, 1, 2):
+                h0 = np.float32(float(_F(d) + (Fraction(k) + Fraction(1, 2)) / _F(inv_e)))
+                for st in range(-48, 49):
+                    h = nudge(h0, st)
+                    if _rint_even(_F(f32_nearest(_F(h) * _F(inv)))) != q:
+                        continue
+                    r = f32_nearest(_F(h) - _F(d))
+                    ea = _rint_even(_F(f32_nearest(_F(r) * _F(inv_e))))
+                    eb = _rint_even(_F(f32_nearest(_F(r) * _F(inv_e_alt))))
+                    if ea != eb:
+                        found = (A, h, ea, eb)
+                        break
+                if found:
+                    break
+            if found:
+                break
+        if found:
+            break
+    assert found, "no distinguishing case found"
+    A, h, ea, eb = found
+    g = np.zeros(block, dtype=np.float32)
+    g[0], g[1] = A, h
+    qe, de = np.zeros(block, np.int8), np.zeros(1, np.float32)
+    oracle.compress_e8(g, qe, de, 1, bits=4, block=block, beta=0.0, kappa=float(kappa))
+    assert qe[1] == ea and ea != eb
+
+
+def test_mean_is_rank_ordered_sum_then_division():
+    """Reading of Eqn (8): mean = RN(RN(RN(d_0 + d_1) + d_2) / 3), the fp32 sum in
+    rank order divided once -- not the sum of per-rank quotients d_w / 3.  Three
+    ranks of one 64-element block whose decoded values make the two orders differ."""
+    rng = np.random.default_rng(8)
+    W, block, bits = 3, 64, 4
+    for _ in range(2000):
+        qs = rng.integers(-8, 8, size=W)
+        ss = rng.uniform(1e-3, 1.0, size=W).astype(np.float32)
+        d = [f32_nearest(int(q) * _F(s)) for q, s in zip(qs, ss)]
+        acc = _F(d[0])
+        for w in range(1, W):
+            acc = _F(f32_nearest(acc + _F(d[w])))
+        want = f32_nearest(acc / W)
+        acc2 = _F(f32_nearest(_F(d[0]) / W))
+        for w in range(1, W):
+            acc2 = _F(f32_nearest(acc2 + _F(f32_nearest(_F(d[w]) / W))))
+        if want != np.float32(float(acc2)):
+            break
+    else:
+        raise AssertionError("no distinguishing case found")
+    codes = []
+    for q in qs:
+        nib = int(q) & 0xF
+        blk = np.zeros(block * bits // 8, dtype=np.uint8)
+        blk[0] = nib                                   # element 0 (low nibble); the rest code 0
+        codes.append(blk)
+    mean = oracle.decode_reduce(codes, [np.array([s], np.float32) for s in ss], block, bits=bits, block=block)
+    assert mean[0].view(np.uint32) == want.view(np.uint32)
+    assert np.all(mean[1:] == 0)
