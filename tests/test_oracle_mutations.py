@@ -59,6 +59,13 @@ MUTATIONS = [
     ("absmax skips the last element", "float amax = 0.0f;\n      for (int64_t j = 0; j < cnt; ++j) {",
      "float amax = 0.0f;\n      for (int64_t j = 0; j < cnt - 1; ++j) {", 0),
     ("m accumulates g*g", "float mg = omb1 * g;", "float mg = omb1 * (g * g);", 0),
+    ("reset applied before compensation", "h[j] = g + err[lo + j];", "h[j] = g + (reset ? 0.0f : err[lo + j]);", 0),
+    ("eps dropped inside the root", "float s = vs + eps;", "float s = vs;", 0),
+    ("weight decay without lr", "const float lr_wd = lr * wd;", "const float lr_wd = wd;", 0),
+    ("nibbles decoded unsigned", "return nib >= 8 ? nib - 16 : nib;", "return nib;", 0),
+    ("symmetric clamp at -qmax", "float qmin = -(float)(1 << (bits - 1));", "float qmin = -qmax;", 0),
+    ("int8 error coded with the gradient code width", "int qe = round_pbit(xe, 8);", "int qe = round_pbit(xe, bits);", 0),
+    ("int8 error not reset", "if (reset) qe = 0;", "if (0) qe = 0;", 0),
 ]
 
 
@@ -95,14 +102,31 @@ def source():
         return f.read()
 
 
-def test_unmodified_oracle_passes(source, tmp_path):
-    so = _build(source, str(tmp_path), "loco_oracle_copy")
-    rc, out = _run_pins(so)
+@pytest.fixture(scope="module")
+def outcomes(source, tmp_path_factory):
+    """Pin-run exit status of the unmodified copy and of every mutant, computed
+    concurrently (each is an independent gcc build plus a pytest subprocess)."""
+    import concurrent.futures as cf
+    d = str(tmp_path_factory.mktemp("mutants"))
+    jobs = {"unmodified": source}
+    for i, (name, old, new, occurrence) in enumerate(MUTATIONS):
+        jobs[name] = _mutate(source, old, new, occurrence)
+
+    def one(item):
+        k, (name, text) = item
+        return name, _run_pins(_build(text, d, f"loco_oracle_{k}"))
+
+    workers = max(1, min(8, (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 4)))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        return dict(ex.map(one, enumerate(jobs.items())))
+
+
+def test_unmodified_oracle_passes(outcomes):
+    rc, out = outcomes["unmodified"]
     assert rc == 0, out
 
 
 @pytest.mark.parametrize("name,old,new,occurrence", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_is_caught(source, tmp_path, name, old, new, occurrence):
-    so = _build(_mutate(source, old, new, occurrence), str(tmp_path), "loco_oracle_mut")
-    rc, out = _run_pins(so)
+def test_planted_mistake_is_caught(outcomes, name, old, new, occurrence):
+    rc, out = outcomes[name]
     assert rc != 0, f"no pin caught the planted mistake: {name}\n{out}"

@@ -676,3 +676,22 @@ def test_mean_is_rank_ordered_sum_then_division():
     mean = oracle.decode_reduce(codes, [np.array([s], np.float32) for s in ss], block, bits=bits, block=block)
     assert mean[0].view(np.uint32) == want.view(np.uint32)
     assert np.all(mean[1:] == 0)
+
+
+def test_adam_eps_inside_the_root_closed_form():
+    """The pages' form of Eqn (9), eps inside the root: den = sqrt(v_hat + eps).
+    A dyadic first step: beta1 = beta2 = 1/2 (both corrections exactly 2), one
+    rank with g = 1/2, eps = 3/4, lr = 1/16: m = 1/4, v = 1/8, v_hat = 1/4,
+    den = sqrt(1/4 + 3/4) = 1, step = lr * 2 * (1/4) = 1/32, so p = 1 - 1/32
+    exactly.  Elements with g = 0 keep p, m and v."""
+    bits, block, n = 4, 64, 64
+    codes = np.zeros(block * bits // 8, dtype=np.uint8)
+    codes[0] = 0x01                                    # element 0: q = 1; the rest q = 0
+    scales = np.array([0.5], np.float32)              # g_0 = 1 * 1/2
+    p = np.ones(n, np.float32)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    oracle.adam_step([codes], [scales], n, p, m, v, 1, bits=bits, block=block, lr=1 / 16, beta1=0.5, beta2=0.5,
+                     eps=0.75, weight_decay=0.0, bias_correction=True, eps_inside_sqrt=True)
+    assert p[0] == np.float32(1 - 1 / 32) and m[0] == np.float32(0.25) and v[0] == np.float32(0.125)
+    assert np.all(p[1:] == 1) and np.all(m[1:] == 0) and np.all(v[1:] == 0)
