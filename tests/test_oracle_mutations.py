@@ -66,6 +66,12 @@ MUTATIONS = [
     ("symmetric clamp at -qmax", "float qmin = -(float)(1 << (bits - 1));", "float qmin = -qmax;", 0),
     ("int8 error coded with the gradient code width", "int qe = round_pbit(xe, 8);", "int qe = round_pbit(xe, bits);", 0),
     ("int8 error not reset", "if (reset) qe = 0;", "if (0) qe = 0;", 0),
+    ("8-bit codes decoded unsigned", "if (bits == 8) return (int)(int8_t)blk[j];", "if (bits == 8) return (int)blk[j];", 0),
+    ("8-bit code sign bit dropped", "blk[j] = (uint8_t)(q & 0xFF);", "blk[j] = (uint8_t)(q & 0x7F);", 0),
+    ("bias correction at t+1", "double bc1 = 1.0 - pow((double)beta1, (double)t);",
+     "double bc1 = 1.0 - pow((double)beta1, (double)(t + 1));", 0),
+    ("v correction without its square root",
+     "c2 = eps_inside_sqrt ? (float)(1.0 / bc2) : (float)(1.0 / sqrt(bc2));", "c2 = (float)(1.0 / bc2);", 0),
 ]
 
 
