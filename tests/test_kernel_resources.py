@@ -1,0 +1,79 @@
+"""Compile-time resource checks of the kernels (no GPU needed).
+
+Each translation unit is compiled for sm_103a with the library's own flags
+plus -Xptxas -v, and the assembler's per-kernel report is checked: no kernel
+spills registers or uses a stack frame, and the kernels whose measured
+occupancy depends on their register count stay within it (the int8-error
+sender at 64 registers = 4 CTAs of 256 threads per SM; Adam within its launch
+bound of 3 CTAs per SM, 85 registers).
+"""
+import concurrent.futures as cf
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+from bit_gradient_compression_gb300 import build as B
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+ENTRY = re.compile(r"Compiling entry function '([^']+)'")
+STACK = re.compile(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads")
+REGS = re.compile(r"Used (\d+) registers")
+
+
+@pytest.fixture(scope="module")
+def report(tmp_path_factory):
+    """{mangled kernel name: (registers, stack bytes, spill store bytes, spill load bytes)}"""
+    out_dir = tmp_path_factory.mktemp("ptxas")
+
+    def one(src):
+        cmd = [B.nvcc(), *B.NVCC_FLAGS, "-Xptxas", "-v", "-c", os.path.join(B.CSRC, src),
+               "-o", os.path.join(str(out_dir), src + ".o")]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr[-2000:]
+        return r.stderr
+
+    with cf.ThreadPoolExecutor(len(B.SOURCES)) as ex:
+        logs = list(ex.map(one, B.SOURCES))
+    kernels, cur = {}, None
+    for log in logs:
+        for line in log.splitlines():
+            m = ENTRY.search(line)
+            if m:
+                cur = m.group(1)
+                kernels[cur] = [None, None, None, None]
+                continue
+            if cur is None:
+                continue
+            m = STACK.search(line)
+            if m:
+                kernels[cur][1:] = [int(m.group(1)), int(m.group(2)), int(m.group(3))]
+            m = REGS.search(line)
+            if m:
+                kernels[cur][0] = int(m.group(1))
+    assert kernels, "no kernel report parsed"
+    return {k: tuple(v) for k, v in kernels.items()}
+
+
+def test_every_kernel_reported(report):
+    for family in ("k_compress", "k_decode_reduce", "k_adam", "k_sgd"):
+        assert any(family in k for k in report), family
+    assert all(None not in v for v in report.values())
+
+
+def test_no_spills_no_stack(report):
+    bad = {k: v for k, v in report.items() if v[1] or v[2] or v[3]}
+    assert not bad, bad
+
+
+def test_register_budgets(report):
+    # the int8-error sender: k_compress<bits, block, bf16, E8 = true, fixed, U, EL>,
+    # 2 code widths x 3 blocks x 2 gradient types x 2 scale modes
+    e8 = [(k, v[0]) for k, v in report.items() if re.search(r"k_compressILi\dELi\d+ELb[01]ELb1E", k)]
+    assert len(e8) == 24 and all(r <= 64 for _, r in e8), e8
+    adam = [(k, v[0]) for k, v in report.items() if "k_adam" in k]
+    assert adam and all(r <= 85 for _, r in adam), [a for a in adam if a[1] > 85]
