@@ -138,3 +138,55 @@ def test_rank_argument_errors(L):
 def test_status_strings(L):
     for s in range(5):
         assert L.lib.loco_status_string(s).decode().startswith("LOCO_")
+
+
+def test_binding_marshalling(L):
+    """The binding's own checks, before anything reaches the library."""
+    import torch
+    cfg = L.make_config()
+    t = torch.zeros(64, 4)
+    with pytest.raises(ValueError, match="contiguous"):
+        L.loco_compress(cfg, t.t(), 0x1000, 1, 0x2000, 0x3000, stream=0)        # a transposed view
+    with pytest.raises(ValueError, match="not supported"):
+        L.loco_compress(cfg, torch.zeros(64, dtype=torch.float16), 0x1000, 1, 0x2000, 0x3000, stream=0)
+    with pytest.raises(ValueError, match="same ranks"):
+        L.loco_decode_reduce(cfg, [0x1000, 0x1100], [0x2000], 64, 0x3000, stream=0)
+    # a non-OK status becomes LocoError carrying the status and the library's message
+    with pytest.raises(L.LocoError) as ei:
+        L.loco_decode_reduce(cfg, [0x1000] * 17, [0x2000] * 17, 64, 0x3000, stream=0)
+    assert ei.value.status == L.LOCO_ERR_UNSUPPORTED and "LOCO_ERR_UNSUPPORTED" in str(ei.value)
+    # dtype inference: bf16 and fp32 gradients map to the header's codes
+    assert L._grad_dtype(torch.zeros(1, dtype=torch.bfloat16), None) == L.LOCO_BF16
+    assert L._grad_dtype(torch.zeros(1), None) == L.LOCO_F32
+
+
+def test_config_and_hparams_layout(L, tmp_path):
+    """The ctypes mirrors of loco_config / loco_adam_hparams have the layout a C
+    compiler gives the header's structs: every field's offset and both sizes."""
+    import ctypes
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    structs = {"loco_config": L.loco_config, "loco_adam_hparams": L.loco_adam_hparams}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "loco.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = {}
+    for line in subprocess.check_output([str(exe)], text=True).splitlines():
+        cname, field, val = line.split()
+        got[(cname, field)] = int(val)
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
+    c = L.make_config(bits=8, block=128, beta=0.25, err_scale_mult=6.0, reset_period=512, fixed_scale=2.0 ** 19)
+    assert (c.bits, c.block, c.scale_mode, c.fixed_scale, c.beta, c.err_scale_mult, c.reset_period) == \
+        (8, 128, L.LOCO_SCALE_FIXED, 2.0 ** 19, 0.25, 6.0, 512)
