@@ -124,10 +124,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("adam.cu", "compress.cu", "decode_reduce.cu", "device_common.cuh", "loco_internal.h",
+                  "receiver_common.cuh", "sgd.cu")   # the kernels and their launchers; abi.cu is host validation
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_gradient_compression_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

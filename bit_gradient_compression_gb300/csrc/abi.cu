@@ -159,12 +159,12 @@ using namespace loco;
 extern "C" {
 
 int64_t loco_num_blocks(int64_t n, int32_t block) {
-  if (n <= 0 || block <= 0) return 0;
+  if (n <= 0 || n > LOCO_MAX_N || block <= 0) return 0;
   return (n + block - 1) / block;
 }
 
 int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block) {
-  if (n <= 0 || block <= 0 || bits <= 0) return 0;
+  if (n <= 0 || n > LOCO_MAX_N || block <= 0 || bits <= 0 || bits > 64) return 0;
   return loco_num_blocks(n, block) * block * bits / 8;
 }
 
@@ -203,7 +203,8 @@ static loco_status compress_common(const loco_config* cfg, const void* grad, int
   if (cfg->scale_mode == LOCO_SCALE_FIXED && (!(cfg->fixed_scale > 0.0f) || !isfinite(cfg->fixed_scale)))
     return fail(LOCO_ERR_INVALID_ARG, "fixed_scale = %g must be finite and > 0", cfg->fixed_scale);
   if (cfg->reset_period < 0) return fail(LOCO_ERR_INVALID_ARG, "reset_period = %lld < 0", (long long)cfg->reset_period);
-  if (n < 0) return fail(LOCO_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
+  if (n < 0 || n > LOCO_MAX_N)
+    return fail(LOCO_ERR_INVALID_ARG, "n = %lld outside [0, LOCO_MAX_N = 2^48]", (long long)n);
   if (step < 1) return fail(LOCO_ERR_INVALID_ARG, "step = %lld (1-based)", (long long)step);
   if (n == 0) return LOCO_OK;
 
@@ -276,7 +277,8 @@ loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* const* cod
   if (cfg == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg is NULL");
   loco_status st = check_layout(cfg->bits, cfg->block);
   if (st != LOCO_OK) return st;
-  if (n < 0) return fail(LOCO_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
+  if (n < 0 || n > LOCO_MAX_N)
+    return fail(LOCO_ERR_INVALID_ARG, "n = %lld outside [0, LOCO_MAX_N = 2^48]", (long long)n);
   if (W < 1) return fail(LOCO_ERR_INVALID_ARG, "W = %d (need >= 1)", W);
   if (W > kMaxRanks) return fail(LOCO_ERR_UNSUPPORTED, "W = %d (at most %d)", W, kMaxRanks);
   if (n == 0) return LOCO_OK;
@@ -330,7 +332,8 @@ static loco_status check_common(const loco_config* cfg, int32_t W, int64_t n) {
   if (cfg == nullptr) return fail(LOCO_ERR_INVALID_ARG, "cfg is NULL");
   loco_status st = check_layout(cfg->bits, cfg->block);
   if (st != LOCO_OK) return st;
-  if (n < 0) return fail(LOCO_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
+  if (n < 0 || n > LOCO_MAX_N)
+    return fail(LOCO_ERR_INVALID_ARG, "n = %lld outside [0, LOCO_MAX_N = 2^48]", (long long)n);
   if (W < 1) return fail(LOCO_ERR_INVALID_ARG, "W = %d (need >= 1)", W);
   if (W > kMaxRanks) return fail(LOCO_ERR_UNSUPPORTED, "W = %d (at most %d)", W, kMaxRanks);
   return LOCO_OK;

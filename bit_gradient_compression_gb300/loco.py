@@ -19,6 +19,7 @@ LOCO_OK, LOCO_ERR_INVALID_ARG, LOCO_ERR_UNSUPPORTED, LOCO_ERR_MISALIGNED, LOCO_E
 LOCO_F32, LOCO_BF16 = 0, 1
 LOCO_SCALE_ABSMAX, LOCO_SCALE_FIXED = 0, 1
 LOCO_MAX_RANKS = 16
+LOCO_MAX_N = 1 << 48
 
 EXPORTS = ("loco_num_blocks", "loco_code_bytes", "loco_compress", "loco_compress_e8", "loco_decode_reduce",
            "loco_adam_step", "loco_adam_step_bf16", "loco_sgd_step", "loco_status_string", "loco_last_error")

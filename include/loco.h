@@ -62,7 +62,7 @@ typedef struct CUstream_st* loco_stream_t;
 
 typedef enum {
   LOCO_OK = 0,
-  LOCO_ERR_INVALID_ARG = 1,  /* null pointer, n < 0, W < 1, step < 1, beta outside [0,1], kappa <= 0, bad scale */
+  LOCO_ERR_INVALID_ARG = 1,  /* null pointer, n < 0 or n > LOCO_MAX_N, W < 1, step < 1, beta outside [0,1], kappa <= 0, bad scale */
   LOCO_ERR_UNSUPPORTED = 2,  /* bits not in {4,8}, block not in {64,128,256}, W > LOCO_MAX_RANKS, unknown dtype/mode */
   LOCO_ERR_MISALIGNED = 3,   /* a pointer violates the alignment rule above */
   LOCO_ERR_CUDA = 4          /* the kernel launch failed; see loco_last_error() */
@@ -77,6 +77,11 @@ typedef enum {
 } loco_scale_mode;
 
 #define LOCO_MAX_RANKS 16
+
+/* Largest bucket a call accepts (2^48 elements, far beyond any device memory);
+ * every size the library derives from n then fits in int64_t.  Larger n is
+ * LOCO_ERR_INVALID_ARG, and the size helpers below return 0 for it. */
+#define LOCO_MAX_N ((int64_t)1 << 48)
 
 /* Sender-side hyper-parameters (§3.1-3.2). */
 typedef struct {
@@ -100,10 +105,11 @@ typedef struct {
   int32_t eps_inside_sqrt; /* 1: 1/sqrt(v+eps) as printed in §4; 0: 1/(sqrt(v)+eps) as in Adam  */
 } loco_adam_hparams;
 
-/* nb = ceil(n / block); 0 for n <= 0 or block <= 0. */
+/* nb = ceil(n / block); 0 for n <= 0, n > LOCO_MAX_N or block <= 0. */
 LOCO_API int64_t loco_num_blocks(int64_t n, int32_t block);
 
-/* Bytes of packed codes for a bucket of n elements: nb * block * bits / 8; 0 on bad arguments. */
+/* Bytes of packed codes for a bucket of n elements: nb * block * bits / 8; 0 on bad arguments
+ * (n <= 0, n > LOCO_MAX_N, bits or block <= 0). */
 LOCO_API int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block);
 
 /*

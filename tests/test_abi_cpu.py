@@ -72,6 +72,11 @@ def test_sizes(L):
     assert L.loco_num_blocks(n7b, 256) == 26_321_936
     assert L.loco_code_bytes(n7b, 4, 256) == n7b // 2
     assert L.loco_code_bytes(1 << 31, 8, 64) == 1 << 31
+    # the largest accepted bucket, and beyond it (no int64 overflow anywhere)
+    assert L.loco_num_blocks(L.LOCO_MAX_N, 64) == L.LOCO_MAX_N // 64
+    assert L.loco_code_bytes(L.LOCO_MAX_N, 8, 64) == L.LOCO_MAX_N
+    for n in (L.LOCO_MAX_N + 1, 1 << 62, 2 ** 63 - 1):
+        assert L.loco_num_blocks(n, 256) == 0 and L.loco_code_bytes(n, 8, 256) == 0
 
 
 def _compress(L, cfg, **kw):
@@ -103,6 +108,8 @@ def test_argument_errors(L):
     assert st(cfg=L.make_config(fixed_scale=-1.0)) == L.LOCO_ERR_INVALID_ARG
     assert st(cfg=L.make_config(reset_period=-1)) == L.LOCO_ERR_INVALID_ARG
     assert st(n=-1) == L.LOCO_ERR_INVALID_ARG
+    assert st(n=L.LOCO_MAX_N + 1) == L.LOCO_ERR_INVALID_ARG
+    assert st(n=2 ** 63 - 1) == L.LOCO_ERR_INVALID_ARG
     assert st(step=0) == L.LOCO_ERR_INVALID_ARG
     assert st(grad=0) == L.LOCO_ERR_INVALID_ARG
     assert st(err=0) == L.LOCO_ERR_INVALID_ARG
@@ -123,6 +130,7 @@ def test_rank_argument_errors(L):
     assert dr(0) == L.LOCO_ERR_INVALID_ARG
     assert dr(17) == L.LOCO_ERR_UNSUPPORTED
     assert dr(4, n=-5) == L.LOCO_ERR_INVALID_ARG
+    assert dr(4, n=2 ** 62) == L.LOCO_ERR_INVALID_ARG
     assert dr(4, n=0) == L.LOCO_OK
     assert _status(L, lambda: L.loco_decode_reduce(cfg, [0x1001], [0x2000], 10, 0x3000, stream=0)) == L.LOCO_ERR_MISALIGNED
     ad = lambda W, t=1, hp=hp: _status(L, lambda: L.loco_adam_step(cfg, [0x1000] * W, [0x2000] * W, 100, 0x3000,
@@ -130,6 +138,10 @@ def test_rank_argument_errors(L):
     assert ad(0) == L.LOCO_ERR_INVALID_ARG
     assert ad(17) == L.LOCO_ERR_UNSUPPORTED
     assert ad(2, t=0) == L.LOCO_ERR_INVALID_ARG
+    assert _status(L, lambda: L.loco_adam_step(cfg, [0x1000] * 2, [0x2000] * 2, 2 ** 62, 0x3000, 0x4000, 0x5000,
+                                               hp, 1, stream=0)) == L.LOCO_ERR_INVALID_ARG
+    assert _status(L, lambda: L.loco_sgd_step(cfg, [0x1000] * 2, [0x2000] * 2, 2 ** 62, 0x3000, 0.1,
+                                              stream=0)) == L.LOCO_ERR_INVALID_ARG
     assert ad(2, hp=L.make_adam(beta1=1.0)) == L.LOCO_ERR_INVALID_ARG
     assert ad(2, hp=L.make_adam(eps=-1.0)) == L.LOCO_ERR_INVALID_ARG
     assert ad(2, hp=L.make_adam(lr=float("inf"))) == L.LOCO_ERR_INVALID_ARG
