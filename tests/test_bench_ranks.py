@@ -94,3 +94,28 @@ def test_workload_sizes():
     assert bench.workload("tinyllama").n == 1_100_048_384
     assert bench.workload("mixtral").n == 8 * 3 * 14336 * 4096
     assert bench.workload("flat:26").n == 1 << 26
+
+
+def test_reference_arm_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON
+    line with the keys of the benchmark line, impl = reference, and an e2e
+    object that moves no bytes between host and device."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "flat:18", "--steps", "1",
+                        "--warmup", "1"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "flat-bf16-2^18" and d["config"]["n_elements"] == 1 << 18
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == pytest.approx(d["value"], rel=1e-3)
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["e2e"]["value"] == pytest.approx(d["value"], rel=1e-3)
