@@ -29,14 +29,33 @@ static loco_status fail(loco_status st, const char* fmt, ...) {
   return st;
 }
 
-int persistent_grid(const void* kernel, int threads, size_t smem_bytes) {
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem_bytes);
-  if (sms <= 0) sms = 1;
-  if (per_sm <= 0) per_sm = 1;
-  return sms * per_sm;
+cudaError_t grid_cap(GridCache& cache, const void* kernel, int threads, size_t smem_bytes, int* cap) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < GridCache::kDevices) {
+    const int c = cache.cap[dev].load(std::memory_order_acquire);
+    if (c > 0) {
+      *cap = c;
+      return cudaSuccess;
+    }
+  }
+  // First launch of this kernel on this device: raise its dynamic shared-memory
+  // limit there (the attribute belongs to the device's copy of the kernel) and
+  // size the persistent grid from this device's SM count and occupancy.
+  if (smem_bytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
+    if (e != cudaSuccess) return e;
+  }
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem_bytes);
+  if (e != cudaSuccess) return e;
+  if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidConfiguration;
+  *cap = sms * per_sm;
+  if (dev >= 0 && dev < GridCache::kDevices) cache.cap[dev].store(*cap, std::memory_order_release);
+  return cudaSuccess;
 }
 
 typedef CUresult (*AddressRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);
@@ -140,7 +159,7 @@ static loco_status check_ranks(const loco_config* cfg, const uint8_t* const* cod
     snprintf(names[2 * w], 16, "codes[%d]", w);
     snprintf(names[2 * w + 1], 16, "scales[%d]", w);
     list[(*count)++] = BufCheck{codes[w], cbytes, 16, names[2 * w]};
-    list[(*count)++] = BufCheck{scales[w], sbytes, 4, names[2 * w + 1]};
+    list[(*count)++] = BufCheck{scales[w], sbytes, 16, names[2 * w + 1]};
     out->codes[w] = codes[w];
     out->scales[w] = scales[w];
   }
@@ -215,8 +234,8 @@ static loco_status compress_common(const loco_config* cfg, const void* grad, int
   const size_t ebytes = e8 ? size_t(n) : size_t(n) * 4;
   const void* ebuf = e8 ? static_cast<const void*>(err_codes) : static_cast<const void*>(err);
   BufCheck bufs[5] = {{grad, gbytes, 16, "grad"}, {ebuf, ebytes, 16, e8 ? "err_codes" : "err"},
-                      {codes, cbytes, 16, "codes"}, {scales, sbytes, 4, "scales"},
-                      {err_steps, sbytes, 4, "err_steps"}};
+                      {codes, cbytes, 16, "codes"}, {scales, sbytes, 16, "scales"},
+                      {err_steps, sbytes, 16, "err_steps"}};
   if ((st = check_buffers(bufs, e8 ? 5 : 4)) != LOCO_OK) return st;
   const int nbufs = e8 ? 5 : 4;
   for (int i = 0; i < nbufs; ++i)

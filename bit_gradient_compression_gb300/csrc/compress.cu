@@ -358,7 +358,10 @@ static cudaError_t launch_t(const CompressArgs& a, cudaStream_t s) {
   constexpr int U = E8 ? LOCO_COMPRESS_UNROLL_E8 : LOCO_COMPRESS_UNROLL;
   constexpr int EL = E8 ? LOCO_COMPRESS_ELEMS_E8 : LOCO_COMPRESS_ELEMS;
   const void* fn = reinterpret_cast<const void*>(&k_compress<BITS, BLOCK, BF16, E8, FIXED, U, EL>);
-  static const int cap = persistent_grid(fn, kThreads);
+  static GridCache cache;
+  int cap = 0;
+  const cudaError_t e = grid_cap(cache, fn, kThreads, 0, &cap);
+  if (e != cudaSuccess) return e;
   const int64_t nb = (a.n + BLOCK - 1) / BLOCK;
   const int64_t warps_needed = (nb * BLOCK + 32 * EL - 1) / (32 * EL);
   const int64_t ctas_needed = (warps_needed + kThreads / 32 - 1) / (kThreads / 32);

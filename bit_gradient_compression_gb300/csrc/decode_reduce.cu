@@ -105,7 +105,10 @@ struct DecodeLaunch {
       using SM = DecodeSmem<BITS, W, E>;
       static_assert(SM::kBytes <= 227 * 1024, "staging area exceeds one CTA's shared memory");
       const void* fn = reinterpret_cast<const void*>(&k_decode_reduce<BITS, W, E, SM::S, SM::kBulk>);
-      static const int cap = receiver_grid(fn, SM::kBytes);
+      static GridCache cache;
+      int cap = 0;
+      const cudaError_t e = grid_cap(cache, fn, kThreads, SM::kBytes, &cap);
+      if (e != cudaSuccess) return e;
       k_decode_reduce<BITS, W, E, SM::S, SM::kBulk>
           <<<clamp_grid(a.n, kThreads * E, cap), kThreads, SM::kBytes, s>>>(a, ilog2_int(a.block));
       return cudaGetLastError();

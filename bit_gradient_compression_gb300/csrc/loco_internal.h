@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace loco {
 
 constexpr int kMaxRanks = 16;
@@ -85,7 +87,18 @@ cudaError_t launch_decode_reduce(const ReduceArgs& a, cudaStream_t s);
 cudaError_t launch_adam(const AdamArgs& a, cudaStream_t s);
 cudaError_t launch_sgd(const SgdArgs& a, cudaStream_t s);
 
-// Number of CTAs for a grid-stride kernel: resident CTAs per SM x SMs.
-int persistent_grid(const void* kernel, int threads, size_t smem_bytes = 0);
+// Launch shape of one kernel instantiation, kept per device: resident CTAs per
+// SM x SMs of that device (0 = not yet computed there).
+struct GridCache {
+  static constexpr int kDevices = 64;
+  std::atomic<int> cap[kDevices];
+};
+
+// Grid cap of a persistent grid-stride kernel on the current device.  The
+// first call per device raises the kernel's dynamic shared-memory limit when
+// smem_bytes exceeds the 48 KB default and queries occupancy; a failure of
+// either is returned (and nothing is cached).  Devices with an ordinal beyond
+// GridCache::kDevices are queried on every call.
+cudaError_t grid_cap(GridCache& cache, const void* kernel, int threads, size_t smem_bytes, int* cap);
 
 }  // namespace loco

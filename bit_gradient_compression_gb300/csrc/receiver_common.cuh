@@ -190,13 +190,6 @@ static inline int ilog2_int(int x) {
   return r;
 }
 
-// Resident CTAs/SM x SMs for a receiver kernel with `smem` bytes of staging,
-// computed once per kernel (static local in the caller's instantiation).
-static inline int receiver_grid(const void* fn, size_t smem) {
-  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  return persistent_grid(fn, kThreads, smem);
-}
-
 static inline int clamp_grid(int64_t n, int elems_per_cta, int cap) {
   const int64_t need = (n + elems_per_cta - 1) / elems_per_cta;
   return int(need < cap ? need : cap);

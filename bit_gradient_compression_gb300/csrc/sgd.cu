@@ -76,7 +76,10 @@ struct SgdLaunch {
       static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
       constexpr bool BULK = LOCO_SGD_BULK != 0 && S >= 2;  // one stage: no room to refill behind a bulk store
       const void* fn = reinterpret_cast<const void*>(&k_sgd<BITS, W, E, S, BF16OUT, BULK>);
-      static const int cap = receiver_grid(fn, smem);
+      static GridCache cache;
+      int cap = 0;
+      const cudaError_t e = grid_cap(cache, fn, kThreads, smem, &cap);
+      if (e != cudaSuccess) return e;
       k_sgd<BITS, W, E, S, BF16OUT, BULK><<<clamp_grid(a.n, kThreads * E, cap), kThreads, smem, s>>>(a, ilog2_int(a.block));
       return cudaGetLastError();
     }

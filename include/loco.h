@@ -23,14 +23,20 @@
  *    b*block*bits/8.  4-bit codes are two's-complement nibbles, element 2j of
  *    the block in the low nibble of byte j, element 2j+1 in the high nibble.
  *    8-bit codes are int8.  Padding elements of a ragged last block get code 0.
- *  - Alignment: grad, err, codes, mean, param, m, v must be 16-byte aligned;
- *    scales 4-byte aligned (LOCO_ERR_MISALIGNED otherwise).
+ *  - Alignment: every buffer (grad, err, err_codes, err_steps, codes, scales,
+ *    mean, param, m, v, param_bf16) must be 16-byte aligned
+ *    (LOCO_ERR_MISALIGNED otherwise).  The receivers stage each rank's steps
+ *    with 16-byte copies, so a rank's scales placed at an offset inside a
+ *    larger buffer (an exchange buffer, a shard of a bucket) must start on a
+ *    16-byte boundary: a shard of a bucket starting at a multiple of 4 quant
+ *    blocks does.
  *  - The calls allocate nothing and never synchronise, so they can be captured
  *    in a CUDA graph.  Step counters, the reset decision and the Adam constants
  *    are computed on the host at call time and become part of the captured
  *    launch: a graph captured at step k replays step k.  The first call of each
- *    configuration (bits, block, W, dtype, ...) queries occupancy and sets the
- *    kernel's shared-memory limit once; make it before capturing.
+ *    configuration (bits, block, W, dtype, ...) on each device queries
+ *    occupancy and sets the kernel's shared-memory limit on that device; make
+ *    it before capturing.
  *  - Arithmetic is IEEE binary32, round to nearest even, every product and
  *    every sum rounded on its own (no product is fused into a following add);
  *    the exact operation order of each step is stated at the

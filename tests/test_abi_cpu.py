@@ -116,6 +116,8 @@ def test_argument_errors(L):
     assert st(grad=0x10001) == L.LOCO_ERR_MISALIGNED
     assert st(codes=0x30008) == L.LOCO_ERR_MISALIGNED
     assert st(scales=0x40002) == L.LOCO_ERR_MISALIGNED
+    assert st(scales=0x40004) == L.LOCO_ERR_MISALIGNED
+    assert st(scales=0x40008) == L.LOCO_ERR_MISALIGNED
     # n == 0 is an empty, successful call (nothing is launched or dereferenced)
     assert st(n=0, grad=0, err=0, codes=0, scales=0) == L.LOCO_OK
     # non-device memory is refused before any launch (here: no driver at all)
@@ -145,6 +147,33 @@ def test_rank_argument_errors(L):
     assert ad(2, hp=L.make_adam(beta1=1.0)) == L.LOCO_ERR_INVALID_ARG
     assert ad(2, hp=L.make_adam(eps=-1.0)) == L.LOCO_ERR_INVALID_ARG
     assert ad(2, hp=L.make_adam(lr=float("inf"))) == L.LOCO_ERR_INVALID_ARG
+
+
+def test_scales_must_be_16_byte_aligned(L):
+    """The receivers stage each rank's steps with 16-byte copies, so a scales
+    pointer at 4, 8 or 12 bytes past a 16-byte boundary is refused on the host
+    (nothing is launched) by every entry point that reads or writes steps."""
+    cfg = L.make_config()
+    hp = L.make_adam()
+    st = lambda fn: _status(L, fn)
+    for bad in (0x40004, 0x40008, 0x4000C):
+        # rank 1 of 3 carries the misaligned steps
+        sc = [0x40000, bad, 0x50000]
+        assert st(lambda: L.loco_decode_reduce(cfg, [0x1000] * 3, sc, 100, 0x3000, stream=0)) == L.LOCO_ERR_MISALIGNED
+        assert st(lambda: L.loco_adam_step(cfg, [0x1000] * 3, sc, 100, 0x3000, 0x4000, 0x5000, hp, 1,
+                                           stream=0)) == L.LOCO_ERR_MISALIGNED
+        assert st(lambda: L.loco_adam_step_bf16(cfg, [0x1000] * 3, sc, 100, 0x3000, 0x4000, 0x5000, 0x6000, hp, 1,
+                                                stream=0)) == L.LOCO_ERR_MISALIGNED
+        assert st(lambda: L.loco_sgd_step(cfg, [0x1000] * 3, sc, 100, 0x3000, 0.1, stream=0)) == L.LOCO_ERR_MISALIGNED
+        assert st(lambda: L.loco_sgd_step(cfg, [0x1000] * 3, sc, 100, 0x3000, 0.1, param_bf16=0x6000,
+                                          stream=0)) == L.LOCO_ERR_MISALIGNED
+        # the sender's outputs: steps and the int8 error's per-block steps
+        assert st(lambda: _compress(L, cfg, scales=bad)) == L.LOCO_ERR_MISALIGNED
+        assert st(lambda: L.loco_compress_e8(cfg, 0x10000, 0x20000, bad, 1, 0x30000, 0x40000, n=1000,
+                                             grad_dtype=0, stream=0)) == L.LOCO_ERR_MISALIGNED
+        assert st(lambda: L.loco_compress_e8(cfg, 0x10000, 0x20000, 0x60000, 1, 0x30000, bad, n=1000,
+                                             grad_dtype=0, stream=0)) == L.LOCO_ERR_MISALIGNED
+    assert "16-byte aligned" in L.lib.loco_last_error().decode()
 
 
 def test_status_strings(L):
