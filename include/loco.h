@@ -195,8 +195,11 @@ LOCO_API loco_status loco_decode_reduce(const loco_config* cfg, const uint8_t* c
  * rank's parameters (§4, Eqn 9: the optimizer consumes the averaged low-bit
  * gradient g~ of Eqn 8).  g~_i is formed exactly as in loco_decode_reduce and
  * is never written to memory.  Per element, in this order (Kingma & Ba's Adam
- * with decoupled weight decay, bias corrections folded into the step size and
- * the denominator as in their Algorithm 1):
+ * with decoupled weight decay; the bias corrections of their Algorithm 1,
+ * m_hat = m/(1 - beta1^t) and v_hat = v/(1 - beta2^t), are folded into the
+ * step size and the denominator, as torch.optim.AdamW arranges them, except
+ * that 1/sqrt(1 - beta2^t) is a rounded factor rather than a divisor; the same
+ * update in exact arithmetic, a different rounding in fp32):
  *   p   = p - (lr*wd)*p
  *   m   = beta1*m + (1-beta1)*g~
  *   v   = beta2*v + (1-beta2)*(g~*g~)

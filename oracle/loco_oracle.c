@@ -202,9 +202,14 @@ void oracle_decode_reduce(int bits, int block, const uint8_t* const* codes,
  * Receiver step fused with the optimizer, §4 Eqn (9): the averaged low-bit
  * gradient g~ of Eqn (8) drives one Adam(W) update of param, m, v for the
  * elements [i0, i1).  g~ is formed exactly as in oracle_decode_reduce.
- * The update is Kingma & Ba's Adam with decoupled weight decay, with the bias
- * corrections folded into the step size and the denominator as in their
- * Algorithm 1 (alpha_t = alpha / (1 - beta1^t), sqrt(v_t) / sqrt(1 - beta2^t)):
+ * The update is Kingma & Ba's Adam with decoupled weight decay.  Their
+ * Algorithm 1 divides m by 1 - beta1^t and v by 1 - beta2^t and steps by
+ * lr * m_hat / (sqrt(v_hat) + eps); here the two corrections are folded, the
+ * first into the step size (c1) and the root of the second into the
+ * denominator (c2), the arrangement of torch.optim.AdamW with its division by
+ * sqrt(1 - beta2^t) taken as a product with the rounded reciprocal.  In exact
+ * arithmetic both are the same update (eps stays outside the corrected root);
+ * in fp32 they round differently:
  *   p   = p - (lr*wd)*p
  *   m   = beta1*m + (1-beta1)*g
  *   v   = beta2*v + (1-beta2)*(g*g)

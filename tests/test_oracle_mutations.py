@@ -38,6 +38,12 @@ MUTATIONS = [
     ("SGD step sign flipped", "float p = param[i] - step;", "float p = param[i] + step;", 0),
     ("Adam eps dropped (eps outside the root)", "den = rs + eps;", "den = rs;", 0),
     ("decoupled weight decay dropped", "p = p - decay;", "p = p - 0.0f * decay;", 0),
+    ("Adam bias corrections unfolded (m_hat, v_hat formed first)",
+     "      float r = sqrtf(vi);\n      float rs = r * c2;\n      den = rs + eps;\n    }\n    float ratio = mi / den;\n"
+     "    float step = c1 * ratio;",
+     "      float vh = vi / (float)(1.0 - pow((double)beta2, (double)t));\n      float r = sqrtf(vh);\n"
+     "      den = r + eps;\n    }\n    float ratio = (mi / (float)(1.0 - pow((double)beta1, (double)t))) / den;\n"
+     "    float step = lr * ratio;", 0),
     ("clip upper bound 128 codes", "const float e_hi = 127.0f * delta_e;", "const float e_hi = 128.0f * delta_e;", 0),
     ("padding codes nonzero", "put_code(blk, bits, j, 0);", "put_code(blk, bits, j, 1);", 0),
     ("int8 error decoded with a neighbouring block's step", "const float de_prev = err_steps[b];",

@@ -695,3 +695,65 @@ def test_adam_eps_inside_the_root_closed_form():
                      eps=0.75, weight_decay=0.0, bias_correction=True, eps_inside_sqrt=True)
     assert p[0] == np.float32(1 - 1 / 32) and m[0] == np.float32(0.25) and v[0] == np.float32(0.125)
     assert np.all(p[1:] == 1) and np.all(m[1:] == 0) and np.all(v[1:] == 0)
+
+
+def _f32_sqrt(x: Fraction) -> np.float32:
+    """Correctly rounded fp32 square root of an exact non-negative rational: y is
+    RN(sqrt(x)) iff x lies between the squares of the midpoints around y (a
+    square root of an fp32 value is never exactly a midpoint)."""
+    y = np.float32(np.sqrt(float(x)))
+    for _ in range(4):
+        up, dn = np.nextafter(y, np.float32(np.inf)), np.nextafter(y, np.float32(0))
+        hi = (_F(y) + _F(up)) / 2
+        lo = (_F(y) + _F(dn)) / 2
+        if x > hi * hi:
+            y = up
+        elif x < lo * lo:
+            y = dn
+        else:
+            return y
+    raise AssertionError("square root did not settle")
+
+
+def test_adam_bias_corrections_folded_into_step_and_denominator():
+    """Reading of Eqn (9) (its Adam: the bias corrections of Kingma & Ba's
+    Algorithm 1, m_hat = m/(1-b1^t), v_hat = v/(1-b2^t), step lr*m_hat/(sqrt(v_hat)+eps)).
+    The oracle folds them: den = RN(RN(sqrt(v))*c2) + eps with c2 = RN(1/sqrt(1-b2^t)),
+    step = RN(c1*RN(m/den)) with c1 = RN(lr/(1-b1^t)) -- equal to Algorithm 1 in
+    exact arithmetic, different in fp32.  Built in exact rationals with every
+    operation rounded to fp32, on an element (t = 3, nonzero state) where the two
+    arrangements round to different parameters: the oracle must give the folded one."""
+    b1, b2, lr, eps, t = np.float32(0.9), np.float32(0.95), np.float32(1e-3), np.float32(1e-8), 3
+    bc1, bc2 = 1.0 - float(b1) ** t, 1.0 - float(b2) ** t        # double, as the constants are formed
+    c1, c2 = np.float32(float(lr) / bc1), np.float32(1.0 / np.sqrt(bc2))
+    omb1, omb2 = f32_nearest(1 - _F(b1)), f32_nearest(1 - _F(b2))
+    R = lambda fr: _F(f32_nearest(fr))                            # round an exact value to fp32
+    rng = np.random.default_rng(21)
+    for _ in range(5000):
+        q = int(rng.integers(-8, 8))
+        s = np.float32(rng.uniform(1e-4, 1e-2))
+        p0, m0, v0 = (np.float32(x) for x in (rng.uniform(-1, 1), rng.normal(0, 1e-3), rng.uniform(1e-8, 1e-5)))
+        g = R(q * _F(s))                                          # one rank: mean = d_0 / 1
+        m1 = R(R(_F(b1) * _F(m0)) + R(_F(omb1) * g))
+        v1 = R(R(_F(b2) * _F(v0)) + R(_F(omb2) * R(g * g)))
+        den = R(R(_F(_f32_sqrt(v1)) * _F(c2)) + _F(eps))
+        folded = f32_nearest(_F(p0) - R(_F(c1) * R(m1 / den)))
+        mh = R(m1 / _F(np.float32(bc1)))
+        vh = R(v1 / _F(np.float32(bc2)))
+        den_u = R(_F(_f32_sqrt(vh)) + _F(eps))
+        unfolded = f32_nearest(_F(p0) - R(_F(lr) * R(mh / den_u)))
+        if folded != unfolded:
+            break
+    else:
+        raise AssertionError("no distinguishing case found")
+    bits, block = 4, 64
+    codes = np.zeros(block * bits // 8, dtype=np.uint8)
+    codes[0] = q & 0xF                                            # element 0 carries q; the rest code 0
+    p = np.full(block, p0, np.float32)
+    m = np.zeros(block, np.float32)
+    v = np.zeros(block, np.float32)
+    m[0], v[0] = m0, v0
+    oracle.adam_step([codes], [np.array([s], np.float32)], block, p, m, v, t, bits=bits, block=block, lr=float(lr),
+                     beta1=float(b1), beta2=float(b2), eps=float(eps), weight_decay=0.0)
+    assert m[0] == np.float32(float(m1)) and v[0] == np.float32(float(v1))
+    assert p[0].view(np.uint32) == folded.view(np.uint32), (p[0], folded, unfolded)
