@@ -187,6 +187,26 @@ int64_t loco_code_bytes(int64_t n, int32_t bits, int32_t block) {
   return loco_num_blocks(n, block) * block * bits / 8;
 }
 
+loco_status loco_shard_range(int64_t n, int32_t block, int32_t W, int32_t j, int64_t* lo, int64_t* hi) {
+  if (lo == nullptr || hi == nullptr) return fail(LOCO_ERR_INVALID_ARG, "lo or hi is NULL");
+  if (block != 64 && block != 128 && block != 256)
+    return fail(LOCO_ERR_UNSUPPORTED, "block = %d (supported: 64, 128, 256)", block);
+  if (n < 0 || n > LOCO_MAX_N)
+    return fail(LOCO_ERR_INVALID_ARG, "n = %lld outside [0, LOCO_MAX_N = 2^48]", (long long)n);
+  if (W < 1) return fail(LOCO_ERR_INVALID_ARG, "W = %d (need >= 1)", W);
+  if (W > kMaxRanks) return fail(LOCO_ERR_UNSUPPORTED, "W = %d (at most %d)", W, kMaxRanks);
+  if (j < 0 || j >= W) return fail(LOCO_ERR_INVALID_ARG, "j = %d outside [0, W = %d)", j, W);
+  const int64_t unit = int64_t(4) * block;
+  const int64_t nu = (n + unit - 1) / unit;
+  const int64_t base = nu / W, rem = nu % W;
+  const int64_t u0 = j * base + (j < rem ? j : rem);
+  const int64_t u1 = (j + 1) * base + (j + 1 < rem ? j + 1 : rem);
+  *lo = u0 * unit < n ? u0 * unit : n;
+  *hi = u1 * unit < n ? u1 * unit : n;
+  g_last_error[0] = '\0';
+  return LOCO_OK;
+}
+
 const char* loco_status_string(loco_status s) {
   switch (s) {
     case LOCO_OK: return "LOCO_OK";

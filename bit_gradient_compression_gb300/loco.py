@@ -22,7 +22,8 @@ LOCO_MAX_RANKS = 16
 LOCO_MAX_N = 1 << 48
 
 EXPORTS = ("loco_num_blocks", "loco_code_bytes", "loco_compress", "loco_compress_e8", "loco_decode_reduce",
-           "loco_adam_step", "loco_adam_step_bf16", "loco_sgd_step", "loco_status_string", "loco_last_error")
+           "loco_adam_step", "loco_adam_step_bf16", "loco_sgd_step", "loco_shard_range", "loco_status_string",
+           "loco_last_error")
 
 
 class LocoError(RuntimeError):
@@ -77,6 +78,8 @@ lib.loco_adam_step_bf16.argtypes = [ctypes.POINTER(loco_config), _vp, _vp, _i32,
 lib.loco_adam_step_bf16.restype = ctypes.c_int
 lib.loco_sgd_step.argtypes = [ctypes.POINTER(loco_config), _vp, _vp, _i32, _i64, _vp, _vp, ctypes.c_float, _vp]
 lib.loco_sgd_step.restype = ctypes.c_int
+lib.loco_shard_range.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+lib.loco_shard_range.restype = ctypes.c_int
 lib.loco_status_string.argtypes = [ctypes.c_int]
 lib.loco_status_string.restype = ctypes.c_char_p
 lib.loco_last_error.argtypes = []
@@ -185,3 +188,10 @@ def loco_sgd_step(cfg: loco_config, codes, scales, n: int, param, lr: float, *, 
     W, ca, sa = _rank_arrays(codes, scales)
     _check(lib.loco_sgd_step(ctypes.byref(cfg), ca, sa, W, n, _addr(param), _addr(param_bf16), float(lr),
                              _stream(stream)))
+
+
+def loco_shard_range(n: int, block: int, W: int, j: int) -> tuple[int, int]:
+    """Element range [lo, hi) of shard j of W (the sharded receiver's split of a bucket)."""
+    lo, hi = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.loco_shard_range(n, block, W, j, ctypes.byref(lo), ctypes.byref(hi)))
+    return lo.value, hi.value

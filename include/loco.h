@@ -242,6 +242,31 @@ LOCO_API loco_status loco_sgd_step(const loco_config* cfg, const uint8_t* const*
                           const float* const* scales, int32_t W, int64_t n,
                           float* param, uint16_t* param_bf16, float lr, loco_stream_t stream);
 
+/*
+ * loco_shard_range — shard j of W of a bucket for the sharded receiver of
+ * §3.3 (the all-to-all variant around Eqn 8): every rank compresses its whole
+ * bucket, sends the low-bit codes and steps of shard j to rank j, and rank j
+ * decodes and averages the W slices it receives (loco_decode_reduce, or a
+ * fused optimizer step, on the shard's n_j = hi - lo elements) and updates its
+ * part of the parameters.
+ *
+ * The bucket is cut into units of U = 4*block elements (so every shard starts
+ * on a quant-block boundary and its codes and steps start 16-byte aligned in
+ * the rank's buffers); with nu = ceil(n / U), shard j holds units
+ * [j*base + min(j, rem), (j+1)*base + min(j+1, rem)) where base = nu / W and
+ * rem = nu % W, clipped to n.  Shards are contiguous, in rank order, cover
+ * [0, n) exactly, and differ in length by at most one unit; when nu < W the
+ * last W - nu shards are empty (lo == hi).  Shard j's codes are bytes
+ * [lo*bits/8, lo*bits/8 + loco_code_bytes(hi - lo)) of a rank's codes and its
+ * steps are floats [lo/block, lo/block + ceil((hi - lo)/block)) of its scales.
+ *
+ * lo, hi (host, out): element range of shard j.  Errors: NULL lo or hi,
+ * n < 0 or n > LOCO_MAX_N, W < 1, j outside [0, W) -> LOCO_ERR_INVALID_ARG;
+ * block not in {64, 128, 256} or W > LOCO_MAX_RANKS -> LOCO_ERR_UNSUPPORTED.
+ * Host only: no CUDA call.
+ */
+LOCO_API loco_status loco_shard_range(int64_t n, int32_t block, int32_t W, int32_t j, int64_t* lo, int64_t* hi);
+
 /* Static text for a status code. */
 LOCO_API const char* loco_status_string(loco_status s);
 
