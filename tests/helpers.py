@@ -88,3 +88,40 @@ def code_rows(codes: torch.Tensor, ids: np.ndarray, block: int, bits: int) -> np
 
 def scale_rows(scales: torch.Tensor, ids: np.ndarray) -> np.ndarray:
     return scales.index_select(0, torch.as_tensor(ids, device=scales.device)).cpu().numpy()
+
+
+class Stage:
+    """Page-locked host buffers, reused by name, for chunked whole-bucket
+    comparisons: fetch() copies a device slice into one and returns it as a
+    numpy array (valid until the next fetch under the same name); put() copies
+    a numpy view of a stage buffer back into device storage."""
+
+    def __init__(self):
+        self.bufs = {}
+
+    def _buf(self, name: str, nbytes: int) -> torch.Tensor:
+        b = self.bufs.get(name)
+        if b is None or b.numel() < nbytes:
+            b = torch.empty(max(nbytes, 16), dtype=torch.uint8, pin_memory=True)
+            self.bufs[name] = b
+        return b[:nbytes]
+
+    def fetch(self, name: str, t: torch.Tensor, np_dtype) -> np.ndarray:
+        nbytes = t.numel() * t.element_size()
+        b = self._buf(name, nbytes)
+        b.copy_(t.reshape(-1).view(torch.uint8), non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return b.numpy().view(np_dtype)
+
+    def zeros(self, name: str, count: int, np_dtype) -> np.ndarray:
+        a = self._buf(name, count * np.dtype(np_dtype).itemsize).numpy().view(np_dtype)
+        a[:] = 0
+        return a
+
+    def array(self, name: str, count: int, np_dtype) -> np.ndarray:
+        return self._buf(name, count * np.dtype(np_dtype).itemsize).numpy().view(np_dtype)
+
+    def put(self, dst: torch.Tensor, arr: np.ndarray):
+        src = torch.from_numpy(arr.view(np.uint8))
+        dst.reshape(-1).view(torch.uint8).copy_(src, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
