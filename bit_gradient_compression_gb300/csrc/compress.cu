@@ -37,6 +37,20 @@ __device__ __forceinline__ void st_words(void* p, const uint32_t (&w)[NW]) {
     st_stream(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
 }
 
+#ifndef LOCO_COMPRESS_E8_CVT
+#define LOCO_COMPRESS_E8_CVT 1  // 1: the int8 error code by one saturating round-to-nearest-even conversion
+#endif
+
+// Nearest integer to x, halves to even, saturated to [-128, 127] (one
+// conversion instruction: a float-to-integer conversion clamps to the range of
+// its destination type); the code is the low byte of the result.  Clamping and
+// then rounding give the same integer because both bounds are integers.
+__device__ __forceinline__ uint32_t rint_sat_s8(float x) {
+  uint32_t r;
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
 // Low bytes of four words, in order, as one word.
 __device__ __forceinline__ uint32_t low_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
@@ -126,11 +140,16 @@ __device__ __forceinline__ void compress_chunk(const CompressArgs& a, int64_t e0
     if constexpr (E8) {
       // Eqn (7): e = Round_8-bit(s_e * e~).
       upk2(prod2(v, inv_e2, z), v0, v1);
+#if LOCO_COMPRESS_E8_CVT
+      teq[2 * k] = rint_sat_s8(v0);
+      teq[2 * k + 1] = rint_sat_s8(v1);
+#else
       const f32x2 te = add2(pk2(fminf(fmaxf(v0, -128.0f), 127.0f), fminf(fmaxf(v1, -128.0f), 127.0f)), magic2);
       float te0, te1;
       upk2(te, te0, te1);
       teq[2 * k] = __float_as_uint(te0);
       teq[2 * k + 1] = __float_as_uint(te1);
+#endif
     } else {
       upk2(v, v0, v1);
       v0 = (v0 < elo) ? elo : v0;
@@ -340,6 +359,92 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Staged variant: every warp streams its own full warp tiles (32*EL elements)
+// through S stages of its own shared memory (warp_pipeline): the gradient and
+// the stored error of a tile are copied in as 16-byte cp.async pieces by the
+// warp's lanes, so S-1 tiles per warp are in flight without holding registers.
+// The int8 error's block step of a lane's chunk is read one tile ahead into a
+// register.  Tiles that reach past n (at most the last one) take the direct
+// path above.  Stage layout: the tile's gradient bytes, then its error bytes.
+// ---------------------------------------------------------------------------
+template <bool BF16, bool E8, int EL>
+struct StagedTile {
+  static constexpr int WT = 32 * EL;
+  static constexpr int GB = WT * (BF16 ? 2 : 4);  // gradient bytes per tile
+  static constexpr int EB = WT * (E8 ? 1 : 4);    // error bytes per tile
+  static constexpr int kStage = GB + EB;
+  static constexpr int GJ = GB / 16 / 32, EJ = EB / 16 / 32;  // 16-byte pieces per lane
+  static_assert(GB % 512 == 0 && EB % 512 == 0, "whole pieces for every lane");
+};
+
+#ifndef LOCO_COMPRESS_STAGED_MINB
+#define LOCO_COMPRESS_STAGED_MINB(e8) 3  // CTAs per SM the register budget is fitted for
+#endif
+
+template <int BITS, int BLOCK, bool BF16, bool E8, bool FIXED, int EL, int S>
+__global__ void __launch_bounds__(kThreads, LOCO_COMPRESS_STAGED_MINB(E8)) k_compress_staged(const CompressArgs a) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  using ST = StagedTile<BF16, E8, EL>;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint8_t* wsm = sm + size_t(warp) * S * ST::kStage;
+  const int64_t nb = (a.n + BLOCK - 1) / BLOCK;
+  const int64_t n_pad = nb * BLOCK;
+  const int64_t ntiles = (n_pad + ST::WT - 1) / ST::WT;
+  const int64_t nfull = a.n / ST::WT;  // tiles wholly below n
+  const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const uint8_t* gsrc = static_cast<const uint8_t*>(a.grad) + 16 * lane;
+  const uint8_t* esrc = (E8 ? reinterpret_cast<const uint8_t*>(a.err_codes) : reinterpret_cast<const uint8_t*>(a.err)) +
+                        16 * lane;
+  auto issue = [&](uint8_t* st, int64_t tile) {
+#pragma unroll
+    for (int j = 0; j < ST::GJ; ++j) cp_async16(st + 16 * (lane + 32 * j), gsrc + tile * ST::GB + 512 * j);
+#pragma unroll
+    for (int j = 0; j < ST::EJ; ++j) cp_async16(st + ST::GB + 16 * (lane + 32 * j), esrc + tile * ST::EB + 512 * j);
+  };
+  float step = 0.0f;
+  if constexpr (E8)
+    if (gw < nfull) step = a.err_steps[(gw * ST::WT + lane * EL) / BLOCK];
+  warp_pipeline<S>(wsm, ST::kStage, gw, nw, nfull, issue, [&](const uint8_t* st, int64_t tile) {
+    RawChunk<BF16, E8, EL> r;
+    const uint4* gs = reinterpret_cast<const uint4*>(st + lane * (ST::GB / 32));
+#pragma unroll
+    for (int i = 0; i < RawChunk<BF16, E8, EL>::kG; ++i) r.g[i] = gs[i];
+    const uint4* es = reinterpret_cast<const uint4*>(st + ST::GB + lane * (ST::EB / 32));
+    if constexpr (E8) {
+      if constexpr (EL == 16) {
+        r.e[0] = es[0];
+      } else {
+        const uint2 c = *reinterpret_cast<const uint2*>(es);
+        r.e[0] = make_uint4(c.x, c.y, 0u, 0u);
+      }
+      r.step = step;
+      if (tile + nw < nfull) step = a.err_steps[((tile + nw) * ST::WT + lane * EL) / BLOCK];
+    } else {
+#pragma unroll
+      for (int i = 0; i < EL / 4; ++i) r.e[i] = es[i];
+    }
+    f32x2 g[EL / 2], e[EL / 2];
+    unpack_raw<BF16, E8, EL>(r, a.neg_zero, g, e);
+    compress_chunk<BITS, BLOCK, E8, FIXED, EL>(a, tile * ST::WT + lane * EL, n_pad, lane, g, e);
+  });
+  // The tiles that reach past n: direct loads, one warp per tile.
+  for (int64_t tile = nfull + gw; tile < ntiles; tile += nw) {
+    RawChunk<BF16, E8, EL> r;
+    issue_tile<BF16, E8, BLOCK, EL>(a, tile, ntiles, lane, r);
+    process_tile<BITS, BLOCK, BF16, E8, FIXED, EL>(a, tile, n_pad, lane, r);
+  }
+}
+
+#ifndef LOCO_COMPRESS_STAGES
+#define LOCO_COMPRESS_STAGES 0     // fp32 error: stages of the staged variant (0: direct loads)
+#endif
+#ifndef LOCO_COMPRESS_STAGES_E8
+#define LOCO_COMPRESS_STAGES_E8 6  // int8 error: stages of the staged variant (0: direct loads)
+#endif
+
 #ifndef LOCO_COMPRESS_UNROLL
 #define LOCO_COMPRESS_UNROLL 2     // fp32 error: 48 bytes per lane per warp tile
 #endif
@@ -357,6 +462,22 @@ template <int BITS, int BLOCK, bool BF16, bool E8, bool FIXED>
 static cudaError_t launch_t(const CompressArgs& a, cudaStream_t s) {
   constexpr int U = E8 ? LOCO_COMPRESS_UNROLL_E8 : LOCO_COMPRESS_UNROLL;
   constexpr int EL = E8 ? LOCO_COMPRESS_ELEMS_E8 : LOCO_COMPRESS_ELEMS;
+  constexpr int S = E8 ? LOCO_COMPRESS_STAGES_E8 : LOCO_COMPRESS_STAGES;
+  if constexpr (S >= 2) {
+    constexpr size_t smem = size_t(kThreads / 32) * S * StagedTile<BF16, E8, EL>::kStage;
+    static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
+    const void* fn = reinterpret_cast<const void*>(&k_compress_staged<BITS, BLOCK, BF16, E8, FIXED, EL, S>);
+    static GridCache cache;
+    int cap = 0;
+    const cudaError_t e = grid_cap(cache, fn, kThreads, smem, &cap);
+    if (e != cudaSuccess) return e;
+    const int64_t nb = (a.n + BLOCK - 1) / BLOCK;
+    const int64_t warps_needed = (nb * BLOCK + 32 * EL - 1) / (32 * EL);
+    const int64_t ctas_needed = (warps_needed + kThreads / 32 - 1) / (kThreads / 32);
+    const int grid = int(ctas_needed < cap ? ctas_needed : cap);
+    k_compress_staged<BITS, BLOCK, BF16, E8, FIXED, EL, S><<<grid, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+  }
   const void* fn = reinterpret_cast<const void*>(&k_compress<BITS, BLOCK, BF16, E8, FIXED, U, EL>);
   static GridCache cache;
   int cap = 0;

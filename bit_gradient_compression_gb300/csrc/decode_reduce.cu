@@ -1,9 +1,19 @@
 // Receiver average of Eqn (8) ("LoCo: Low-Bit Communication Adaptor for
-// Large-scale Model Training", §3.3): the W ranks' codes and steps are staged
-// per tile by the cp.async pipeline.  Where the fp32 output carries most of
-// the bytes, each thread writes its E means into a shared-memory output tile
-// and one thread stores the whole tile with a bulk (TMA) copy, so the output
-// leaves in full, contiguous lines; otherwise threads store directly.
+// Large-scale Model Training", §3.3): decode W ranks' packed buckets and
+// average them in fp32, rank order, one division by W.
+//
+// Two kernels, chosen per (bits, W) from measurements over W = 1..16 (2^30
+// elements and the 7B bucket):
+//  * k_decode_reduce (8-bit codes): CTA tiles staged by the cp.async pipeline;
+//    every thread writes its E means into a shared-memory output tile and one
+//    thread ships the tile with a bulk (TMA) store, so the output leaves in
+//    full, contiguous lines.
+//  * k_decode_reduce_wl (4-bit codes, where decoding every code costs more
+//    issue slots per byte): every warp streams its own warp tiles through its
+//    own pipeline stages (warp_pipeline) and never meets the CTA's other warps
+//    at a barrier; each warp ships its tile's means with its own bulk store.
+//    Up to 8 ranks: CTAs of 8 warps with 3 stages; beyond that the stages are
+//    larger, and CTAs of 4 warps with 2 stages keep 4-5 CTAs resident.
 #include "receiver_common.cuh"
 
 namespace loco {
@@ -12,46 +22,53 @@ namespace loco {
 #define LOCO_REDUCE_ELEMS(bits) (64 / (bits))  // elements per thread: 8 code bytes per rank
 #endif
 #ifndef LOCO_REDUCE_MIN_CTAS
-#define LOCO_REDUCE_MIN_CTAS 3  // CTAs per SM the stage count is fitted for
+#define LOCO_REDUCE_MIN_CTAS 3  // CTAs per SM the stage counts are fitted for
 #endif
-
-// Output path and pipeline depth per configuration, from measurements over
-// W = 1..16 at 2^30 elements.  While the fp32 mean dominates the traffic (8-bit
-// codes, or 4-bit codes of up to 4 ranks) it is written through a shared-memory
-// tile and one bulk copy per tile; with 4-bit codes of more ranks the kernel is
-// bound by the per-code decode work, the extra shared-memory pass costs more
-// than it saves, and threads store directly with a deeper load pipeline.
-#ifndef LOCO_REDUCE_BULK_MAX_W4
-#define LOCO_REDUCE_BULK_MAX_W4 4  // largest rank count whose 4-bit mean goes through the bulk store
+#ifndef LOCO_REDUCE_CTA_MAX_W4
+#define LOCO_REDUCE_CTA_MAX_W4 0  // largest rank count whose 4-bit codes take the CTA-tile kernel
 #endif
 #ifndef LOCO_REDUCE_STAGES8
 #define LOCO_REDUCE_STAGES8 2
 #endif
-#ifndef LOCO_REDUCE_STAGES4_BULK
-#define LOCO_REDUCE_STAGES4_BULK 3
+#ifndef LOCO_REDUCE_STAGES4
+#define LOCO_REDUCE_STAGES4 3
 #endif
-#ifndef LOCO_REDUCE_STAGES4_DIRECT
-#define LOCO_REDUCE_STAGES4_DIRECT 4
+#ifndef LOCO_REDUCE_WL_BULK_MAX_W
+#define LOCO_REDUCE_WL_BULK_MAX_W 8  // largest rank count of the warp-local kernel with bulk output stores
 #endif
+#ifndef LOCO_REDUCE_WL_STAGES_BULK
+#define LOCO_REDUCE_WL_STAGES_BULK 3
+#endif
+#ifndef LOCO_REDUCE_WL_WARPS_HI
+#define LOCO_REDUCE_WL_WARPS_HI 4  // warps per CTA of the warp-local kernel beyond LOCO_REDUCE_WL_BULK_MAX_W ranks
+#endif
+#ifndef LOCO_REDUCE_WL_BULK_HI
+#define LOCO_REDUCE_WL_BULK_HI 1  // bulk output stores beyond LOCO_REDUCE_WL_BULK_MAX_W ranks
+#endif
+#ifndef LOCO_REDUCE_WL_MIN_CTAS_HI
+#define LOCO_REDUCE_WL_MIN_CTAS_HI(w) ((w) <= 11 ? 5 : 4)
+#endif
+#ifndef LOCO_REDUCE_WL_STAGES_HI
+#define LOCO_REDUCE_WL_STAGES_HI 2
+#endif
+
 template <int BITS, int W>
-constexpr bool use_bulk_store() {
-  return BITS == 8 || W <= LOCO_REDUCE_BULK_MAX_W4;
-}
-template <int BITS, int W>
-constexpr int wanted_stages() {
-  return BITS == 8 ? LOCO_REDUCE_STAGES8
-                   : (use_bulk_store<BITS, W>() ? LOCO_REDUCE_STAGES4_BULK : LOCO_REDUCE_STAGES4_DIRECT);
+constexpr bool use_warp_local() {
+  return BITS == 4 && W > LOCO_REDUCE_CTA_MAX_W4;
 }
 
+// ---------------------------------------------------------------------------
+// CTA-tile kernel with a bulk output store per tile.
+// ---------------------------------------------------------------------------
 template <int BITS, int W, int E>
 struct DecodeSmem {
-  static constexpr bool kBulk = use_bulk_store<BITS, W>();
-  static constexpr size_t kOut = kBulk ? size_t(kThreads) * E * 4 : 0;  // one output tile
-  static constexpr int S = fit_stages<BITS, W, E, 0>(wanted_stages<BITS, W>(), kOut, LOCO_REDUCE_MIN_CTAS);
+  static constexpr size_t kOut = size_t(kThreads) * E * 4;  // one output tile
+  static constexpr int S =
+      fit_stages<BITS, W, E, 0>(BITS == 8 ? LOCO_REDUCE_STAGES8 : LOCO_REDUCE_STAGES4, kOut, LOCO_REDUCE_MIN_CTAS);
   static constexpr size_t kBytes = size_t(S) * Tile<BITS, W, E, 0>::kBytes + kOut;
 };
 
-template <int BITS, int W, int E, int S, bool BULK>
+template <int BITS, int W, int E, int S>
 __global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, int log2_block) {
   extern __shared__ __align__(16) uint8_t sm[];
   using TL = Tile<BITS, W, E, 0>;
@@ -60,18 +77,13 @@ __global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, 
   const bool leader = threadIdx.x == 0;
   tile_pipeline<BITS, W, E, 0, S>(
       none, a.ranks, a.n, log2_block,
-      [&](const TL& tl, int64_t e0) {
+      [&](const TL& tl, int64_t) {
         float mean[E];
         tile_mean<BITS, W, E, 0>(tl, threadIdx.x, log2_block, a.ranks.neg_zero, mean);
-        if constexpr (BULK) {
-          float4* o = reinterpret_cast<float4*>(out + threadIdx.x * E);
+        float4* o = reinterpret_cast<float4*>(out + threadIdx.x * E);
 #pragma unroll
-          for (int q = 0; q < E / 4; ++q)
-            o[q] = make_float4(mean[4 * q], mean[4 * q + 1], mean[4 * q + 2], mean[4 * q + 3]);
-          fence_smem_to_async_proxy();  // make the tile visible to the bulk copy
-        } else {
-          store_vec<E>(a.mean, e0, a.n, true, mean);
-        }
+        for (int q = 0; q < E / 4; ++q) o[q] = make_float4(mean[4 * q], mean[4 * q + 1], mean[4 * q + 2], mean[4 * q + 3]);
+        fence_smem_to_async_proxy();  // make the tile visible to the bulk copy
       },
       [&](int64_t e0) {
         float mean[E];
@@ -80,20 +92,138 @@ __global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, 
       },
       // before a tile is published: the previous tile's bulk store has read `out`
       [&](int64_t) {
-        if constexpr (BULK)
-          if (leader) bulk_wait_read_all();
+        if (leader) bulk_wait_read_all();
       },
       // after every thread wrote `out`: one thread ships it
       [&](int64_t tile) {
-        if constexpr (BULK) {
-          if (leader) {
-            bulk_store(a.mean + tile * TL::T, out, uint32_t(TL::T * 4));
-            bulk_commit();
-          }
+        if (leader) {
+          bulk_store(a.mean + tile * TL::T, out, uint32_t(TL::T * 4));
+          bulk_commit();
         }
       });
+  if (leader) bulk_wait_all();
+}
+
+// ---------------------------------------------------------------------------
+// Warp-local kernel: every warp streams its own warp tiles of WT = 32*E
+// elements through S stages of its own shared memory (warp_pipeline).  A stage
+// holds the W ranks' packed codes of one warp tile (W * WT*BITS/8 bytes, rank
+// major), copied as 16-byte pieces by the warp's lanes; the W steps a lane
+// needs (one block per lane: E <= block) are read one tile ahead into
+// registers.  With BULK each warp writes its tile's means into its own output
+// tile in shared memory and lane 0 ships it with one bulk (TMA) store; the next
+// tile's means go there only after that store has read it.
+// ---------------------------------------------------------------------------
+template <int BITS, int W, int E, bool BULK, int WARPS>
+struct WarpTile {
+  static constexpr int kWarps = WARPS;
+  static constexpr int WT = 32 * E;                      // elements per warp tile
+  static constexpr int CB = WT * BITS / 8;               // code bytes per rank and warp tile
+  static constexpr int kPieces = CB / 16;                // 16-byte pieces per rank
+  static constexpr int kJobs = (W * kPieces + 31) / 32;  // pieces per lane
+  static constexpr size_t kStage = size_t(W) * CB;
+  static constexpr size_t kOut = BULK ? size_t(WT) * 4 : 0;  // per-warp output tile
+  static_assert(CB % 16 == 0, "whole 16-byte pieces");
+  static constexpr size_t bytes(int st) { return size_t(kWarps) * (st * kStage + kOut); }
+  // Largest stage count <= want (>= 2) for which min_ctas CTAs fit on one SM.
+  static constexpr int stages(int want, int min_ctas) {
+    int st = want;
+    while (st > 2 && (size_t(min_ctas) * (bytes(st) + 1024) > size_t(228) * 1024 || bytes(st) > size_t(227) * 1024))
+      --st;
+    return st;
+  }
+};
+
+// Configuration of the warp-local kernel for W ranks: CTA size, output path,
+// stage count, and the CTAs per SM its shared memory and registers are fitted for.
+template <int BITS, int W, int E>
+struct WarpLocalConfig {
+  static constexpr bool kLow = W <= LOCO_REDUCE_WL_BULK_MAX_W;
+  static constexpr int kWarps = kLow ? 8 : LOCO_REDUCE_WL_WARPS_HI;
+  static constexpr bool kBulk = kLow ? true : (LOCO_REDUCE_WL_BULK_HI != 0);
+  static constexpr int kMinCtas = kLow ? LOCO_REDUCE_MIN_CTAS : LOCO_REDUCE_WL_MIN_CTAS_HI(W);
+  using WTL = WarpTile<BITS, W, E, kBulk, kWarps>;
+  static constexpr int S = WTL::stages(kLow ? LOCO_REDUCE_WL_STAGES_BULK : LOCO_REDUCE_WL_STAGES_HI, kMinCtas);
+  static constexpr size_t kSmem = WTL::bytes(S);
+  static_assert(kSmem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
+};
+
+template <int BITS, int W, int E>
+__global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, WarpLocalConfig<BITS, W, E>::kMinCtas)
+    k_decode_reduce_wl(const ReduceArgs a, int log2_block) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  using CF = WarpLocalConfig<BITS, W, E>;
+  using WTL = typename CF::WTL;
+  constexpr int S = CF::S;
+  constexpr bool BULK = CF::kBulk;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint8_t* wsm = sm + size_t(warp) * S * WTL::kStage;
+  float* wout = reinterpret_cast<float*>(sm + size_t(WTL::kWarps) * S * WTL::kStage) + size_t(warp) * WTL::WT;
+  const int64_t gw = int64_t(blockIdx.x) * WTL::kWarps + warp;
+  const int64_t nw = int64_t(gridDim.x) * WTL::kWarps;
+  const int64_t ntiles = a.n / WTL::WT;
+
+  // This lane's pieces of every tile: piece p = lane + 32*j is piece p % kPieces
+  // of rank p / kPieces; it lands at byte 16*p of the stage (rank-major, CB =
+  // 16*kPieces) and comes from the same offset of every tile (plus tile*CB).
+  const uint8_t* src[WTL::kJobs];
+#pragma unroll
+  for (int j = 0; j < WTL::kJobs; ++j) {
+    const int p = lane + 32 * j;
+    src[j] = (p < W * WTL::kPieces) ? a.ranks.codes[p / WTL::kPieces] + 16 * (p % WTL::kPieces) : nullptr;
+  }
+  auto issue = [&](uint8_t* st, int64_t tile) {
+#pragma unroll
+    for (int j = 0; j < WTL::kJobs; ++j)
+      if ((W * WTL::kPieces) % 32 == 0 || lane + 32 * j < W * WTL::kPieces)
+        cp_async16(st + 16 * (lane + 32 * j), src[j] + tile * WTL::CB);
+  };
+  // Steps of this lane's block for every rank, one tile ahead in registers.
+  float sc[W];
+  auto load_steps = [&](float (&s)[W], int64_t tile) {
+    const int64_t blk = (tile * WTL::WT + int64_t(lane) * E) >> log2_block;
+#pragma unroll
+    for (int w = 0; w < W; ++w) s[w] = __ldg(a.ranks.scales[w] + blk);
+  };
+  if (gw < ntiles) load_steps(sc, gw);
+  warp_pipeline<S>(wsm, WTL::kStage, gw, nw, ntiles, issue, [&](const uint8_t* st, int64_t tile) {
+    float nsc[W];
+    if (tile + nw < ntiles) load_steps(nsc, tile + nw);
+    ChunkCodes<BITS, E> cw[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) cw[w].load_shared(st + w * WTL::CB + lane * (E * BITS / 8));
+    float mean[E];
+    mean_of_codes<BITS, W, E>(cw, sc, a.ranks.neg_zero, mean);
+    if constexpr (BULK) {
+      if (lane == 0) bulk_wait_read_all();  // the previous tile's store has read the output tile
+      __syncwarp();
+      float4* o = reinterpret_cast<float4*>(wout + lane * E);
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) o[q] = make_float4(mean[4 * q], mean[4 * q + 1], mean[4 * q + 2], mean[4 * q + 3]);
+      fence_smem_to_async_proxy();  // this lane's means visible to the bulk copy
+      __syncwarp();
+      if (lane == 0) {
+        bulk_store(a.mean + tile * WTL::WT, wout, uint32_t(WTL::WT * 4));
+        bulk_commit();
+      }
+    } else {
+      store_vec<E>(a.mean, tile * WTL::WT + int64_t(lane) * E, a.n, true, mean);
+    }
+#pragma unroll
+    for (int w = 0; w < W; ++w) sc[w] = nsc[w];
+  });
   if constexpr (BULK)
-    if (leader) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
+  // Elements past the last full warp tile: one warp, straight from global memory.
+  if (ntiles * WTL::WT < a.n && gw == ntiles % nw) {
+    const int64_t e0 = ntiles * WTL::WT + int64_t(lane) * E;
+    if (e0 < a.n) {
+      float mean[E];
+      decode_mean<BITS, W, E>(a.ranks, e0, e0 >> log2_block, mean);
+      store_vec<E>(a.mean, e0, a.n, e0 + E <= a.n, mean);
+    }
+  }
 }
 
 template <int BITS>
@@ -102,15 +232,31 @@ struct DecodeLaunch {
   struct F {
     static cudaError_t run(const ReduceArgs& a, cudaStream_t s) {
       constexpr int E = LOCO_REDUCE_ELEMS(BITS);
-      using SM = DecodeSmem<BITS, W, E>;
-      static_assert(SM::kBytes <= 227 * 1024, "staging area exceeds one CTA's shared memory");
-      const void* fn = reinterpret_cast<const void*>(&k_decode_reduce<BITS, W, E, SM::S, SM::kBulk>);
+      const void* fn;
+      size_t smem;
+      int threads = kThreads;
+      if constexpr (use_warp_local<BITS, W>()) {
+        using CF = WarpLocalConfig<BITS, W, E>;
+        fn = reinterpret_cast<const void*>(&k_decode_reduce_wl<BITS, W, E>);
+        smem = CF::kSmem;
+        threads = CF::kWarps * 32;
+      } else {
+        using SM = DecodeSmem<BITS, W, E>;
+        static_assert(SM::kBytes <= 227 * 1024, "staging area exceeds one CTA's shared memory");
+        fn = reinterpret_cast<const void*>(&k_decode_reduce<BITS, W, E, SM::S>);
+        smem = SM::kBytes;
+      }
       static GridCache cache;
       int cap = 0;
-      const cudaError_t e = grid_cap(cache, fn, kThreads, SM::kBytes, &cap);
+      const cudaError_t e = grid_cap(cache, fn, threads, smem, &cap);
       if (e != cudaSuccess) return e;
-      k_decode_reduce<BITS, W, E, SM::S, SM::kBulk>
-          <<<clamp_grid(a.n, kThreads * E, cap), kThreads, SM::kBytes, s>>>(a, ilog2_int(a.block));
+      const int grid = clamp_grid(a.n, threads * E, cap);
+      if constexpr (use_warp_local<BITS, W>()) {
+        k_decode_reduce_wl<BITS, W, E><<<grid, threads, smem, s>>>(a, ilog2_int(a.block));
+      } else {
+        using SM = DecodeSmem<BITS, W, E>;
+        k_decode_reduce<BITS, W, E, SM::S><<<grid, kThreads, smem, s>>>(a, ilog2_int(a.block));
+      }
       return cudaGetLastError();
     }
   };

@@ -156,6 +156,43 @@ __device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, 
 }
 
 // ---------------------------------------------------------------------------
+// Warp-local multistage pipeline.  Warp gw of nw walks its own tiles gw,
+// gw + nw, ... through S stages of its own shared memory (wsm), S-1 tiles in
+// flight while one is consumed.  The warp's lanes copy a tile together
+// (cp.async), so cp.async.wait_group (each lane's own copies landed) plus
+// __syncwarp (memory ordering among the warp's lanes) make it visible to every
+// lane; the __syncwarp also guarantees that the stage refilled next, the one
+// consumed in the previous iteration, is no longer being read.  No CTA-wide
+// barrier and no spin-wait: warps of a CTA drift freely.  Every lane of the
+// warp must run this with the same arguments.
+//   issue(stage_base, tile): start this lane's share of the tile's copies
+//   body(stage_base, tile):  consume one staged tile
+// ---------------------------------------------------------------------------
+template <int S, typename Issue, typename Body>
+__device__ __forceinline__ void warp_pipeline(uint8_t* wsm, size_t stage_bytes, int64_t gw, int64_t nw, int64_t ntiles,
+                                              Issue issue, Body body) {
+  static_assert(S >= 2, "one stage computes while the next loads");
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    const int64_t tile = gw + int64_t(s) * nw;
+    if (tile < ntiles) issue(wsm + s * stage_bytes, tile);
+    cp_async_commit();
+  }
+  int cur = 0;
+  for (int64_t tile = gw; tile < ntiles; tile += nw) {
+    cp_async_wait<S - 2>();  // this lane's copies of `tile` have landed
+    __syncwarp();            // ... and every other lane's; the previous stage is free
+    const int prev = (cur == 0) ? S - 1 : cur - 1;
+    const int64_t ahead = tile + int64_t(S - 1) * nw;
+    if (ahead < ntiles) issue(wsm + prev * stage_bytes, ahead);
+    cp_async_commit();
+    body(wsm + cur * stage_bytes, tile);
+    cur = (cur + 1 == S) ? 0 : cur + 1;
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
 // Packed fp32 pairs.  add.rn.f32x2 / mul.rn.f32x2 / fma.rn.f32x2 (sm_100+)
 // each round every lane exactly like the scalar instruction and issue once per
 // pair.  A packed multiply whose result feeds a packed add, however, was
@@ -217,7 +254,7 @@ __device__ __forceinline__ f32x2 prod2(f32x2 a, f32x2 b, f32x2 neg_zero2) {
 template <int BITS, int E>
 struct ChunkCodes {
   static constexpr int kWords = E * BITS / 32;  // 32-bit words per rank
-  static_assert(kWords == 1 || kWords == 2, "one 4- or 8-byte load per rank");
+  static_assert(kWords == 1 || kWords == 2 || kWords == 4, "one 4-, 8- or 16-byte load per rank");
   uint32_t w[kWords];
 
   static constexpr int kBytes = kWords * 4;
@@ -226,20 +263,32 @@ struct ChunkCodes {
     const uint8_t* p = base + (e0 * BITS >> 3);
     if constexpr (kWords == 1) {
       w[0] = ld_stream(reinterpret_cast<const uint32_t*>(p));
-    } else {
+    } else if constexpr (kWords == 2) {
       const uint2 v = ld_stream(reinterpret_cast<const uint2*>(p));
       w[0] = v.x;
       w[1] = v.y;
+    } else {
+      const uint4 v = ld_stream(reinterpret_cast<const uint4*>(p));
+      w[0] = v.x;
+      w[1] = v.y;
+      w[2] = v.z;
+      w[3] = v.w;
     }
   }
 
   __device__ __forceinline__ void load_shared(const uint8_t* src) {
     if constexpr (kWords == 1) {
       w[0] = *reinterpret_cast<const uint32_t*>(src);
-    } else {
+    } else if constexpr (kWords == 2) {
       const uint2 v = *reinterpret_cast<const uint2*>(src);
       w[0] = v.x;
       w[1] = v.y;
+    } else {
+      const uint4 v = *reinterpret_cast<const uint4*>(src);
+      w[0] = v.x;
+      w[1] = v.y;
+      w[2] = v.z;
+      w[3] = v.w;
     }
   }
 
@@ -269,18 +318,88 @@ struct ChunkCodes {
   }
 };
 
-// Division by W of a pair of sums: for a power of two, multiplying by the
-// exact reciprocal gives the same correctly rounded quotient; otherwise an
-// IEEE division per lane.
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Division of the rank sum by W, correctly rounded like the IEEE division.
+//  * W a power of two: the product with the exact reciprocal is the same
+//    correctly rounded quotient.
+//  * otherwise: the division by a constant known in advance of Brisebarre,
+//    Muller and Raina ("Accelerating correctly rounded floating-point division
+//    when the divisor is known in advance", IEEE Trans. Computers 53(8),
+//    2004): q = fma(x, zh, RN(x*zl)) with zh the binary32 number just below
+//    1/W and zl = RN(1/W - zh) > 0, two packed instructions per pair.  For
+//    W = 3..15 it equals RN(x/W) for every binary32 x with |x| >= 2^-100
+//    (checked exhaustively over all such x); it can differ only where x*zl
+//    underflows.  With zl > 0 a zero sum keeps its sign (+-0 / W = +-0).
+//    The sums are never that small unless a step is: when every rank's step of
+//    the block is 0 or at least 2^-77, every decoded term RN(q*Delta) is 0 or
+//    a normal number of magnitude >= 2^-77, hence a multiple of 2^-100, and so
+//    is every rounded partial sum (a rounded sum of multiples of 2^-100 stays
+//    one), so a nonzero sum has |x| >= 2^-100.  A block with a nonzero step
+//    below 2^-77 takes the IEEE division instead.
+// ---------------------------------------------------------------------------
+
+// Largest binary32 number not above 1/W (W >= 3, not a power of two).
+constexpr float recip_below(int W) {
+  float f = 1.0f / float(W);
+  if (double(f) > 1.0 / double(W)) {
+    double e = 1.0;
+    while (e > double(f)) e *= 0.5;  // 2^floor(log2 f)
+    f = float(double(f) - e * 1.1920928955078125e-07);  // one unit in the last place below
+  }
+  return f;
+}
+
 template <int W>
-__device__ __forceinline__ void div_by_ranks(f32x2 sum, float& lo, float& hi) {
-  if constexpr ((W & (W - 1)) == 0) {
-    upk2(mul2(sum, pk2(1.0f / float(W), 1.0f / float(W))), lo, hi);
+struct RankDiv {
+  static constexpr bool kPow2 = (W & (W - 1)) == 0;
+  static constexpr float zh = kPow2 ? 1.0f / float(W) : recip_below(W);
+  static constexpr float zl = kPow2 ? 0.0f : float(1.0 / double(W) - double(zh));
+};
+
+// True when every step is 0 or at least 2^-77 (the fast quotient is exact):
+// no step's magnitude lies in (0, 2^-77), i.e. none has bits in [1, bits(2^-77)).
+template <int W>
+__device__ __forceinline__ bool steps_allow_fast_division(const float (&s)[W]) {
+  constexpr uint32_t kMinBits = 0x19000000u;  // bits of 2^-77
+  uint32_t small = 0;
+#pragma unroll
+  for (int w = 0; w < W; ++w) small |= uint32_t((__float_as_uint(s[w]) & 0x7FFFFFFFu) - 1u < kMinBits - 1u);
+  return small == 0;
+}
+
+// Two-constant quotient of a pair (W not a power of two).
+template <int W>
+__device__ __forceinline__ void div_fast(f32x2 sum, float& lo, float& hi) {
+  using D = RankDiv<W>;
+  upk2(fma2(sum, pk2(D::zh, D::zh), mul2(sum, pk2(D::zl, D::zl))), lo, hi);
+}
+
+// The quotients of E/2 pairs of rank sums (see RankDiv).
+template <int W, int E>
+__device__ __forceinline__ void div_by_ranks(const f32x2 (&acc)[E / 2], const float (&s)[W], float out[E]) {
+  using D = RankDiv<W>;
+  if constexpr (D::kPow2) {
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j) upk2(mul2(acc[j], pk2(D::zh, D::zh)), out[2 * j], out[2 * j + 1]);
   } else {
-    float a, b;
-    upk2(sum, a, b);
-    lo = __fdiv_rn(a, float(W));
-    hi = __fdiv_rn(b, float(W));
+    if (steps_allow_fast_division<W>(s)) {
+#pragma unroll
+      for (int j = 0; j < E / 2; ++j) div_fast<W>(acc[j], out[2 * j], out[2 * j + 1]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < E / 2; ++j) {
+        float a, b;
+        upk2(acc[j], a, b);
+        out[2 * j] = __fdiv_rn(a, float(W));
+        out[2 * j + 1] = __fdiv_rn(b, float(W));
+      }
+    }
   }
 }
 
@@ -304,8 +423,7 @@ __device__ __forceinline__ void mean_of_codes(const ChunkCodes<BITS, E> (&cw)[W]
       acc[j] = (w == 0) ? d : add2(acc[j], d);
     }
   }
-#pragma unroll
-  for (int j = 0; j < E / 2; ++j) div_by_ranks<W>(acc[j], out[2 * j], out[2 * j + 1]);
+  div_by_ranks<W, E>(acc, s, out);
 }
 
 // Same, loading the codes straight from global memory (chunk at e0, block blk).

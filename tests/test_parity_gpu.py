@@ -169,6 +169,57 @@ def test_decode_reduce_parity(L, W, bits, block):
         assert mean.intact()
 
 
+@pytest.mark.parametrize("W", [3, 5, 6, 7, 12, 15])
+@pytest.mark.parametrize("bits,block", [(4, 64), (8, 128)])
+def test_decode_reduce_small_steps_and_signed_zeros(L, W, bits, block):
+    """Division by a rank count that is not a power of two: the kernels take a
+    two-constant quotient when every step of a block is 0 or >= 2^-77 and the
+    IEEE division otherwise.  Blocks whose steps include tiny normal and
+    subnormal values (one rank or all), zero steps with negative codes (decoded
+    terms -0, so zero sums of either sign) and ordinary steps; mean and the
+    fused Adam step bit-exact against the oracle."""
+    n = 64 * block + 17
+    nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(70 + W)
+    codes = [torch.randint(0, 256, (cb,), dtype=torch.uint8, device=DEV, generator=gen) for _ in range(W)]
+    tiny = torch.tensor([2.0 ** -77, 2.0 ** -78, 2.0 ** -100, 2.0 ** -126, 2.0 ** -140, 1e-45], device=DEV)
+    scales = []
+    for w in range(W):
+        sc = torch.rand(nb, device=DEV, generator=gen) * 1e-3
+        k = torch.arange(nb, device=DEV)
+        sc = torch.where(k % 8 == 1, tiny[k % 6], sc)                          # one tiny step per block...
+        sc = torch.where((k % 8 == 2) & (w == W - 1), tiny[(k + w) % 6], sc)   # ...or only the last rank's
+        sc = torch.where(k % 8 == 3, torch.zeros_like(sc), sc)                 # zero steps: terms +-0
+        sc = torch.where((k % 8 == 4) & (w % 2 == 0), torch.zeros_like(sc), sc)
+        scales.append(sc)
+    # blocks 5 mod 8: every rank's codes negative with a zero step, so the sum is -0
+    bpb = block * bits // 8
+    for c, sc in zip(codes, scales):
+        cv = c.view(nb, bpb)
+        neg = 0x99 if bits == 4 else 0x80
+        cv[5::8] = neg
+        sc[5::8] = 0.0
+    mean = torch.empty(n, device=DEV)
+    cfg = L.make_config(bits=bits, block=block)
+    L.loco_decode_reduce(cfg, codes, scales, n, mean)
+    ch, sh = [c.cpu().numpy() for c in codes], [x.cpu().numpy() for x in scales]
+    om = oracle.decode_reduce(ch, sh, n, bits=bits, block=block)
+    torch.cuda.synchronize()
+    got = mean.cpu().numpy()
+    assert_bits_equal(got, om, f"mean W={W}")
+    assert np.signbit(got.reshape(-1)[5 * block]) and got.reshape(-1)[5 * block] == 0
+    p = wl().fill_uniform(torch.empty(n, device=DEV), 4, -0.1, 0.1)
+    m, v = torch.zeros(n, device=DEV), torch.zeros(n, device=DEV)
+    ph, mh, vh = p.cpu().numpy().copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    hpk = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)
+    L.loco_adam_step(cfg, codes, scales, n, p, m, v, L.make_adam(**hpk), 1)
+    oracle.adam_step(ch, sh, n, ph, mh, vh, 1, bits=bits, block=block, **hpk)
+    torch.cuda.synchronize()
+    for got_t, want, name in ((p, ph, "param"), (m, mh, "m"), (v, vh, "v")):
+        assert_bits_equal(got_t.cpu().numpy(), want, f"{name} W={W}")
+
+
 @pytest.mark.parametrize("W", [1, 3, 8, 16])
 @pytest.mark.parametrize("bits,block", [(4, 256), (8, 64)])
 @pytest.mark.parametrize("variant", ["adamw", "paper", "plain"])
