@@ -15,9 +15,14 @@ flush is needed between steps.
 
 value = gradient bytes processed per second: compress counts N*2 bytes (bf16
 gradient), decode-reduce and the fused Adam each count W*N*2 bytes (the
-gradient-equivalent of the W contributions they consume).  Each kernel's
-roofline fraction is algorithmic HBM bytes / its CUDA-event time / the
-measured HBM copy bandwidth.
+gradient-equivalent of the W contributions they consume).  Decode-reduce and
+the fused Adam decode the same W packed buffers, so those W*N*2 bytes are
+counted twice, and the mean that decode-reduce writes is not consumed inside
+the timed step (the fused step re-derives it): value is the metric's
+definitional sum, not a traffic figure.  The traffic figures are each
+kernel's roofline fraction (algorithmic HBM bytes / its CUDA-event time / the
+measured HBM copy bandwidth) and, for the whole step, "step_hbm": all
+kernels' algorithmic bytes / ms_per_step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl loco|reference]
 
@@ -56,6 +61,8 @@ def parse():
     ap.add_argument("--workload", default="llama2-7b",
                     help="llama2-7b (default), tinyllama, mixtral, or flat:<log2 n> (bf16, 4-bit, block 256, W 8)")
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="host-to-device copy streams of the end-to-end leg (inputs split across them)")
     ap.add_argument("--error-storage", default="fp32", choices=["fp32", "int8"],
                     help="compensation error kept in fp32 (default) or as int8 codes + per-block step")
     ap.add_argument("--optimizer", default="adam", choices=["adam", "sgd"],
@@ -371,7 +378,8 @@ def run_e2e(args, L, w, cfg, n, nb, cb, g, compress, update, codes, scales, mean
     W = len(codes)
     dev = g.device
     comp = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    nS = max(1, args.e2e_copy_streams)
+    s_ins, s_out = [torch.cuda.Stream() for _ in range(nS)], torch.cuda.Stream()
     hosts = []
 
     def host_like(t):
@@ -412,35 +420,74 @@ def run_e2e(args, L, w, cfg, n, nb, cb, g, compress, update, codes, scales, mean
             torch.cuda.synchronize()
             best = max(best, probe_n / (a0.elapsed_time(b0) * 1e-3) / 1e9)
         link.append(best)
+    # the whole input set of one step, copied once as the loop copies it (one pass per buffer, in
+    # order, on the first copy stream): what the loop's inputs alone take on this machine
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(s_ins[0])
+    with torch.cuda.stream(s_ins[0]):
+        sets[1][0].copy_(g_h, non_blocking=True)
+        for r in range(1, W):
+            sets[1][1][r].copy_(codes_h[r - 1], non_blocking=True)
+            sets[1][2][r].copy_(scales_h[r - 1], non_blocking=True)
+    b0.record(s_ins[0])
+    torch.cuda.synchronize()
+    full_set_GBps = h2d / (a0.elapsed_time(b0) * 1e-3) / 1e9
+    # the same link with the copy split over the copy streams, as the loop issues it
+    parts = [(i * probe_n // nS, (i + 1) * probe_n // nS) for i in range(nS)]
+    best = 0.0
+    for _ in range(3):
+        a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(comp)
+        for st, (lo, hi) in zip(s_ins, parts):
+            st.wait_event(a0)
+            with torch.cuda.stream(st):
+                dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+        for st in s_ins:
+            comp.wait_stream(st)
+        b0.record(comp)
+        torch.cuda.synchronize()
+        best = max(best, probe_n / (a0.elapsed_time(b0) * 1e-3) / 1e9)
+    link.append(best)
     g.copy_(g_h)
     torch.cuda.synchronize()
     K = args.e2e_steps
     ev = lambda: torch.cuda.Event()
-    g_done, in_done, comp_done, c0_done, out_done = [[ev() for _ in range(K)] for _ in range(5)]
+    comp_done, c0_done, out_done = [[ev() for _ in range(K)] for _ in range(3)]
+    g_done, in_done = [[[ev() for _ in range(nS)] for _ in range(K)] for _ in range(2)]
+    # each copy stream takes one contiguous part of the gradient, then its share of ranks 1..W-1
+    gparts = [(i * n // nS, (i + 1) * n // nS) for i in range(nS)]
     if world > 1:
         dist.barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(comp)
-    s_in.wait_event(a)
+    for st in s_ins:
+        st.wait_event(a)
     s_out.wait_event(a)
     for k in range(K):
         gk, ck, sk = sets[k % 2]
-        with torch.cuda.stream(s_in):          # inputs of step k
-            if k >= 2:
-                s_in.wait_event(comp_done[k - 2])
-            gk.copy_(g_h, non_blocking=True)
-            g_done[k].record(s_in)
-            for r in range(1, W):
+        for i, st in enumerate(s_ins):         # inputs of step k
+            with torch.cuda.stream(st):
+                if k >= 2:
+                    st.wait_event(comp_done[k - 2])
+                lo, hi = gparts[i]
+                gk[lo:hi].copy_(g_h[lo:hi], non_blocking=True)
+                g_done[k][i].record(st)
+        for r in range(1, W):
+            st = s_ins[(r - 1) % nS]
+            with torch.cuda.stream(st):
                 ck[r].copy_(codes_h[r - 1], non_blocking=True)
                 sk[r].copy_(scales_h[r - 1], non_blocking=True)
-            in_done[k].record(s_in)
-        comp.wait_event(g_done[k])
+        for i, st in enumerate(s_ins):
+            in_done[k][i].record(st)
+        for e_ in g_done[k]:
+            comp.wait_event(e_)
         if k >= 2:
             comp.wait_event(out_done[k - 2])   # rank 0's buffer of set k % 2 has left
         compress(gk, k + 1, ck[0], sk[0], stream=comp)
         c0_done[k].record(comp)
-        comp.wait_event(in_done[k])            # ranks 1..W-1 arrived
+        for e_ in in_done[k]:
+            comp.wait_event(e_)                # ranks 1..W-1 arrived
         L.loco_decode_reduce(cfg, ck, sk, n, mean, stream=comp)
         update(ck, sk, k + 1, stream=comp)
         comp_done[k].record(comp)
@@ -450,14 +497,15 @@ def run_e2e(args, L, w, cfg, n, nb, cb, g, compress, update, codes, scales, mean
             out_s.copy_(sk[0], non_blocking=True)
             out_done[k].record(s_out)
     comp.wait_event(out_done[K - 1])
-    comp.wait_event(in_done[K - 1])
+    for e_ in in_done[K - 1]:
+        comp.wait_event(e_)
     b.record(comp)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / K
     for h in hosts:
         torch.cuda.cudart().cudaHostUnregister(h.data_ptr())
     del sets[1]
-    return (ms, h2d, d2h, link)
+    return (ms, h2d, d2h, link + [full_set_GBps])
 
 
 def run_loco(args, rank, world):
@@ -601,6 +649,7 @@ def run_loco(args, rank, world):
     hbm, hbm_kind = peaks()
     default_step = not e8 and opt == "adam" and pb16 is None and args.fixed_scale is None
     kb = kernel_bytes(n, gsize, bits, block, W, e8, opt, pb16 is not None)
+    step_bytes = sum(kb.values())
     roof = {}
     for k, ms in per_kernel.items():
         ach = kb[k] / (ms * 1e-3) / 1e9
@@ -628,6 +677,9 @@ def run_loco(args, rank, world):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU, W ranks simulated in HBM"},
         "roofline": dict(roof[dominant], kernel=dominant),
         "roofline_kernels": roof,
+        "step_hbm": {"algorithmic_bytes": step_bytes, "achieved": round(step_bytes / (t_ms * 1e-3) / 1e9, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(step_bytes / (t_ms * 1e-3) / 1e9 / hbm, 4),
+                     "what": "algorithmic HBM bytes of all kernels of one step / ms_per_step"},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
     }
@@ -639,12 +691,16 @@ def run_loco(args, rank, world):
         out["e2e"] = {"value": round(whole_job_value(units_step, world, e2e_ms), 1), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                       "steps": args.e2e_steps,
-                      "host_link_GBps": {"h2d": round(link[0], 1), "d2h": round(link[1], 1)},
-                      "copy_bound_ms_per_step": round(h2d / (link[0] * 1e9) * 1e3, 1),
+                      "host_link_GBps": {"h2d": round(link[0], 1), "d2h": round(link[1], 1),
+                                         f"h2d_{args.e2e_copy_streams}_streams": round(link[2], 1),
+                                         "h2d_step_inputs": round(link[3], 1)},
+                      "copy_streams": args.e2e_copy_streams,
+                      "copy_bound_ms_per_step": round(h2d / (max(link[0], link[2]) * 1e9) * 1e3, 1),
                       "achieved_h2d_GBps": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
-                      "what": "page-locked host -> device: rank 0 gradient + ranks 1..W-1 packed buffers; "
-                              "device -> page-locked host: rank 0's packed buffer; copies on their own streams "
-                              "overlap the previous step's kernels (double-buffered device inputs)"}
+                      "what": "page-locked host -> device: rank 0 gradient + ranks 1..W-1 packed buffers "
+                              "(split over the copy streams); device -> page-locked host: rank 0's packed buffer; "
+                              "copies on their own streams overlap the previous step's kernels (double-buffered "
+                              "device inputs)"}
     return out
 
 
