@@ -341,8 +341,14 @@ __device__ __forceinline__ void process_tile(const CompressArgs& a, int64_t t, i
 // lane whose chunk crosses n (only in the last warp tile) loads it element by
 // element instead.  The register budget is the compiler's default for 256
 // threads (a minimum-CTA launch bound lets it grow and costs occupancy).
+#ifdef LOCO_COMPRESS_MINB  // CTAs per SM the direct-load sender's register budget is fitted for
+#define LOCO_COMPRESS_BOUNDS __launch_bounds__(kThreads, LOCO_COMPRESS_MINB)
+#else  // the compiler's default budget for 256 threads
+#define LOCO_COMPRESS_BOUNDS __launch_bounds__(kThreads)
+#endif
+
 template <int BITS, int BLOCK, bool BF16, bool E8, bool FIXED, int U, int EL>
-__global__ void __launch_bounds__(kThreads) k_compress(const CompressArgs a) {
+__global__ void LOCO_COMPRESS_BOUNDS k_compress(const CompressArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t nb = (a.n + BLOCK - 1) / BLOCK;
   const int64_t n_pad = nb * BLOCK;

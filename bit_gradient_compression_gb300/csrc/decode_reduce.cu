@@ -51,6 +51,12 @@ namespace loco {
 #ifndef LOCO_REDUCE_WL_STAGES_HI
 #define LOCO_REDUCE_WL_STAGES_HI 2
 #endif
+#ifndef LOCO_REDUCE_WL_STEPS_SMEM
+// Rank counts whose tiles stage their steps with the codes (cp.async) instead
+// of reading them one tile ahead into registers: measured faster at W = 1 and
+// W > 8, slower at W = 2..8.
+#define LOCO_REDUCE_WL_STEPS_SMEM(w) ((w) == 1 || (w) > 8)
+#endif
 
 template <int BITS, int W>
 constexpr bool use_warp_local() {
@@ -110,18 +116,23 @@ __global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, 
 // holds the W ranks' packed codes of one warp tile (W * WT*BITS/8 bytes, rank
 // major), copied as 16-byte pieces by the warp's lanes; the W steps a lane
 // needs (one block per lane: E <= block) are read one tile ahead into
-// registers.  With BULK each warp writes its tile's means into its own output
+// registers (or, for the rank counts LOCO_REDUCE_WL_STEPS_SMEM names, copied
+// into the stage with the codes as 8-byte pieces).  With BULK each warp writes
+// its tile's means into its own output
 // tile in shared memory and lane 0 ships it with one bulk (TMA) store; the next
 // tile's means go there only after that store has read it.
 // ---------------------------------------------------------------------------
-template <int BITS, int W, int E, bool BULK, int WARPS>
+template <int BITS, int W, int E, bool BULK, int WARPS, bool STEPS_SMEM>
 struct WarpTile {
   static constexpr int kWarps = WARPS;
+  static constexpr bool kStepsSmem = STEPS_SMEM;
   static constexpr int WT = 32 * E;                      // elements per warp tile
   static constexpr int CB = WT * BITS / 8;               // code bytes per rank and warp tile
   static constexpr int kPieces = CB / 16;                // 16-byte pieces per rank
   static constexpr int kJobs = (W * kPieces + 31) / 32;  // pieces per lane
-  static constexpr size_t kStage = size_t(W) * CB;
+  static constexpr int kStepsMax = WT / 64;                  // steps per rank and tile, smallest block
+  static constexpr size_t kStepBytes = STEPS_SMEM ? size_t(W) * kStepsMax * 4 : 0;
+  static constexpr size_t kStage = size_t(W) * CB + kStepBytes;
   static constexpr size_t kOut = BULK ? size_t(WT) * 4 : 0;  // per-warp output tile
   static_assert(CB % 16 == 0, "whole 16-byte pieces");
   static constexpr size_t bytes(int st) { return size_t(kWarps) * (st * kStage + kOut); }
@@ -142,7 +153,7 @@ struct WarpLocalConfig {
   static constexpr int kWarps = kLow ? 8 : LOCO_REDUCE_WL_WARPS_HI;
   static constexpr bool kBulk = kLow ? true : (LOCO_REDUCE_WL_BULK_HI != 0);
   static constexpr int kMinCtas = kLow ? LOCO_REDUCE_MIN_CTAS : LOCO_REDUCE_WL_MIN_CTAS_HI(W);
-  using WTL = WarpTile<BITS, W, E, kBulk, kWarps>;
+  using WTL = WarpTile<BITS, W, E, kBulk, kWarps, bool(LOCO_REDUCE_WL_STEPS_SMEM(W))>;
   static constexpr int S = WTL::stages(kLow ? LOCO_REDUCE_WL_STAGES_BULK : LOCO_REDUCE_WL_STAGES_HI, kMinCtas);
   static constexpr size_t kSmem = WTL::bytes(S);
   static_assert(kSmem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
@@ -173,11 +184,33 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
     const int p = lane + 32 * j;
     src[j] = (p < W * WTL::kPieces) ? a.ranks.codes[p / WTL::kPieces] + 16 * (p % WTL::kPieces) : nullptr;
   }
+  // With the steps staged: a tile's nsc steps per rank are 8-byte pieces
+  // (nsc/2 per rank, W*nsc/2 <= 64 in all), at most two per lane.
+  const int nsc = WTL::WT >> log2_block;
+  const float* ssrc[2];
+  uint32_t sdst[2];
+  bool sval[2];
+  if constexpr (WTL::kStepsSmem) {
+    const int half = nsc >> 1;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int p = lane + 32 * j;
+      sval[j] = p < W * half;
+      const int w = sval[j] ? p / half : 0, k = sval[j] ? p % half : 0;
+      ssrc[j] = a.ranks.scales[w] + 2 * k;
+      sdst[j] = uint32_t(W * WTL::CB + (w * WTL::kStepsMax + 2 * k) * 4);
+    }
+  }
   auto issue = [&](uint8_t* st, int64_t tile) {
 #pragma unroll
     for (int j = 0; j < WTL::kJobs; ++j)
       if ((W * WTL::kPieces) % 32 == 0 || lane + 32 * j < W * WTL::kPieces)
         cp_async16(st + 16 * (lane + 32 * j), src[j] + tile * WTL::CB);
+    if constexpr (WTL::kStepsSmem) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (sval[j]) cp_async8(st + sdst[j], ssrc[j] + tile * nsc);
+    }
   };
   // Steps of this lane's block for every rank, one tile ahead in registers.
   float sc[W];
@@ -186,10 +219,17 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
 #pragma unroll
     for (int w = 0; w < W; ++w) s[w] = __ldg(a.ranks.scales[w] + blk);
   };
-  if (gw < ntiles) load_steps(sc, gw);
+  if constexpr (!WTL::kStepsSmem)
+    if (gw < ntiles) load_steps(sc, gw);
   warp_pipeline<S>(wsm, WTL::kStage, gw, nw, ntiles, issue, [&](const uint8_t* st, int64_t tile) {
-    float nsc[W];
-    if (tile + nw < ntiles) load_steps(nsc, tile + nw);
+    float nsc_[W];
+    if constexpr (WTL::kStepsSmem) {
+      const float* ss = reinterpret_cast<const float*>(st + W * WTL::CB) + ((lane * E) >> log2_block);
+#pragma unroll
+      for (int w = 0; w < W; ++w) sc[w] = ss[w * WTL::kStepsMax];
+    } else {
+      if (tile + nw < ntiles) load_steps(nsc_, tile + nw);
+    }
     ChunkCodes<BITS, E> cw[W];
 #pragma unroll
     for (int w = 0; w < W; ++w) cw[w].load_shared(st + w * WTL::CB + lane * (E * BITS / 8));
@@ -210,8 +250,10 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
     } else {
       store_vec<E>(a.mean, tile * WTL::WT + int64_t(lane) * E, a.n, true, mean);
     }
+    if constexpr (!WTL::kStepsSmem) {
 #pragma unroll
-    for (int w = 0; w < W; ++w) sc[w] = nsc[w];
+      for (int w = 0; w < W; ++w) sc[w] = nsc_[w];
+    }
   });
   if constexpr (BULK)
     if (lane == 0) bulk_wait_all();

@@ -50,6 +50,10 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+// 8-byte copy (cached in L1 on the way), both addresses 8-byte aligned.
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -292,7 +296,11 @@ struct ChunkCodes {
     }
   }
 
-  // q2[j] holds elements (2j, 2j+1) as floats q exactly.
+  // Elements held by pair j of decode().
+  __host__ __device__ static constexpr int pair_lo(int j) { return 2 * j; }
+  __host__ __device__ static constexpr int pair_hi(int j) { return 2 * j + 1; }
+
+  // q2[j] holds elements (pair_lo(j), pair_hi(j)) as floats q exactly.
   __device__ __forceinline__ void decode(f32x2 q2[E / 2]) const {
     constexpr uint32_t K = 0x4B000000u;
     if constexpr (BITS == 4) {
@@ -380,24 +388,25 @@ __device__ __forceinline__ void div_fast(f32x2 sum, float& lo, float& hi) {
   upk2(fma2(sum, pk2(D::zh, D::zh), mul2(sum, pk2(D::zl, D::zl))), lo, hi);
 }
 
-// The quotients of E/2 pairs of rank sums (see RankDiv).
-template <int W, int E>
+// The quotients of E/2 pairs of rank sums (see RankDiv); pair j holds the
+// elements (CC::pair_lo(j), CC::pair_hi(j)) of the chunk.
+template <int W, int E, typename CC>
 __device__ __forceinline__ void div_by_ranks(const f32x2 (&acc)[E / 2], const float (&s)[W], float out[E]) {
   using D = RankDiv<W>;
   if constexpr (D::kPow2) {
 #pragma unroll
-    for (int j = 0; j < E / 2; ++j) upk2(mul2(acc[j], pk2(D::zh, D::zh)), out[2 * j], out[2 * j + 1]);
+    for (int j = 0; j < E / 2; ++j) upk2(mul2(acc[j], pk2(D::zh, D::zh)), out[CC::pair_lo(j)], out[CC::pair_hi(j)]);
   } else {
     if (steps_allow_fast_division<W>(s)) {
 #pragma unroll
-      for (int j = 0; j < E / 2; ++j) div_fast<W>(acc[j], out[2 * j], out[2 * j + 1]);
+      for (int j = 0; j < E / 2; ++j) div_fast<W>(acc[j], out[CC::pair_lo(j)], out[CC::pair_hi(j)]);
     } else {
 #pragma unroll
       for (int j = 0; j < E / 2; ++j) {
         float a, b;
         upk2(acc[j], a, b);
-        out[2 * j] = __fdiv_rn(a, float(W));
-        out[2 * j + 1] = __fdiv_rn(b, float(W));
+        out[CC::pair_lo(j)] = __fdiv_rn(a, float(W));
+        out[CC::pair_hi(j)] = __fdiv_rn(b, float(W));
       }
     }
   }
@@ -423,7 +432,7 @@ __device__ __forceinline__ void mean_of_codes(const ChunkCodes<BITS, E> (&cw)[W]
       acc[j] = (w == 0) ? d : add2(acc[j], d);
     }
   }
-  div_by_ranks<W, E>(acc, s, out);
+  div_by_ranks<W, E, ChunkCodes<BITS, E>>(acc, s, out);
 }
 
 // Same, loading the codes straight from global memory (chunk at e0, block blk).
