@@ -37,7 +37,7 @@ namespace loco {
 #define LOCO_REDUCE_WL_BULK_MAX_W 8  // largest rank count of the warp-local kernel with bulk output stores
 #endif
 #ifndef LOCO_REDUCE_WL_STAGES_BULK
-#define LOCO_REDUCE_WL_STAGES_BULK 3
+#define LOCO_REDUCE_WL_STAGES_BULK(w) 3  // stages up to LOCO_REDUCE_WL_BULK_MAX_W ranks (5 or 6 at W <= 4: no faster)
 #endif
 #ifndef LOCO_REDUCE_WL_WARPS_HI
 #define LOCO_REDUCE_WL_WARPS_HI 4  // warps per CTA of the warp-local kernel beyond LOCO_REDUCE_WL_BULK_MAX_W ranks
@@ -114,13 +114,13 @@ __global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, 
 // Warp-local kernel: every warp streams its own warp tiles of WT = 32*E
 // elements through S stages of its own shared memory (warp_pipeline).  A stage
 // holds the W ranks' packed codes of one warp tile (W * WT*BITS/8 bytes, rank
-// major), copied as 16-byte pieces by the warp's lanes; the W steps a lane
+// major), copied as 16-byte pieces by the warp's lanes.  The W steps a lane
 // needs (one block per lane: E <= block) are read one tile ahead into
-// registers (or, for the rank counts LOCO_REDUCE_WL_STEPS_SMEM names, copied
-// into the stage with the codes as 8-byte pieces).  With BULK each warp writes
-// its tile's means into its own output
-// tile in shared memory and lane 0 ships it with one bulk (TMA) store; the next
-// tile's means go there only after that store has read it.
+// registers, or, for the rank counts LOCO_REDUCE_WL_STEPS_SMEM names, copied
+// into the stage after the codes as 8-byte pieces.  With BULK each warp writes
+// its tile's means into its own output tile in shared memory and lane 0 ships
+// it with one bulk (TMA) store; the next tile's means go there only after that
+// store has read it.
 // ---------------------------------------------------------------------------
 template <int BITS, int W, int E, bool BULK, int WARPS, bool STEPS_SMEM>
 struct WarpTile {
@@ -154,7 +154,7 @@ struct WarpLocalConfig {
   static constexpr bool kBulk = kLow ? true : (LOCO_REDUCE_WL_BULK_HI != 0);
   static constexpr int kMinCtas = kLow ? LOCO_REDUCE_MIN_CTAS : LOCO_REDUCE_WL_MIN_CTAS_HI(W);
   using WTL = WarpTile<BITS, W, E, kBulk, kWarps, bool(LOCO_REDUCE_WL_STEPS_SMEM(W))>;
-  static constexpr int S = WTL::stages(kLow ? LOCO_REDUCE_WL_STAGES_BULK : LOCO_REDUCE_WL_STAGES_HI, kMinCtas);
+  static constexpr int S = WTL::stages(kLow ? LOCO_REDUCE_WL_STAGES_BULK(W) : LOCO_REDUCE_WL_STAGES_HI, kMinCtas);
   static constexpr size_t kSmem = WTL::bytes(S);
   static_assert(kSmem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
 };

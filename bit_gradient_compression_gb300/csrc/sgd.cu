@@ -11,7 +11,11 @@ namespace loco {
 #define LOCO_SGD_ELEMS(bits) (64 / (bits))
 #endif
 #ifndef LOCO_SGD_MIN_CTAS
-#define LOCO_SGD_MIN_CTAS 3  // CTAs per SM the stage count is fitted for (measured best)
+// CTAs per SM the stage count is fitted for (measured best).  For 9..12 ranks
+// of 4-bit codes three CTAs would leave room for one unpipelined stage; two
+// CTAs with two stages measured faster there (W = 12: 81 % -> 88 %), but not
+// at 13..16 ranks (W = 16: 93 % with three CTAs, 87 % with two).
+#define LOCO_SGD_MIN_CTAS(bits, w) ((bits) == 4 && (w) > 8 && (w) <= 12 ? 2 : 3)
 #endif
 #ifndef LOCO_SGD_STAGES
 #define LOCO_SGD_STAGES 3
@@ -71,7 +75,7 @@ struct SgdLaunch {
   struct F {
     static cudaError_t run(const SgdArgs& a, cudaStream_t s) {
       constexpr int E = LOCO_SGD_ELEMS(BITS);
-      constexpr int S = fit_stages<BITS, W, E, 1>(LOCO_SGD_STAGES, 0, LOCO_SGD_MIN_CTAS);
+      constexpr int S = fit_stages<BITS, W, E, 1>(LOCO_SGD_STAGES, 0, LOCO_SGD_MIN_CTAS(BITS, W));
       constexpr size_t smem = S * Tile<BITS, W, E, 1>::kBytes;
       static_assert(smem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
       constexpr bool BULK = LOCO_SGD_BULK != 0 && S >= 2;  // one stage: no room to refill behind a bulk store
