@@ -131,14 +131,21 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("adam.cu", "compress.cu", "decode_reduce.cu", "device_common.cuh", "loco_internal.h",
-                  "receiver_common.cuh", "sgd.cu")   # the kernels and their launchers; abi.cu is host validation
+# The sources each timed kernel (and its launcher) is built from; abi.cu is host validation.
+_COMMON = ("device_common.cuh", "loco_internal.h")
+KERNEL_SOURCES = {
+    "compress": ("compress.cu",) + _COMMON,
+    "decode_reduce": ("decode_reduce.cu", "receiver_common.cuh") + _COMMON,
+    "adam": ("adam.cu", "receiver_common.cuh") + _COMMON,
+    "sgd": ("sgd.cu", "receiver_common.cuh") + _COMMON,
+}
 
 
-def source_hash() -> str:
+def source_hash(kernel: str) -> str:
+    """Hash of the sources one kernel is built from (stored with its ncu counters)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_gradient_compression_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -154,8 +161,8 @@ def ncu_traffic(kernel: str, units: int, n_elems: int, workload_name: str):
             d = json.load(f)
     except Exception:
         return None
-    if (d.get("source_hash") != source_hash() or d.get("workload") != workload_name
-            or d.get("n_elements") != n_elems or kernel not in d.get("kernels", {})):
+    if (d.get("workload") != workload_name or d.get("n_elements") != n_elems or kernel not in d.get("kernels", {})
+            or d["kernels"][kernel].get("source_hash") != source_hash(kernel)):
         return None
     return d["kernels"][kernel]["dram_bytes"]
 
