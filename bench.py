@@ -141,13 +141,27 @@ KERNEL_SOURCES = {
 }
 
 
-def source_hash(kernel: str) -> str:
-    """Hash of the sources one kernel is built from (stored with its ncu counters)."""
+def code_of(text: str) -> str:
+    """C/C++ source with comments removed and whitespace collapsed: what a change
+    to a kernel's code alters and a change to its comments does not."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def source_hash(kernel: str, read=None) -> str:
+    """Hash of the code (comments aside) of the sources one kernel is built from,
+    stored with its ncu counters.  read(name) -> text overrides reading the file."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_gradient_compression_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        if read is None:
+            with open(os.path.join(csrc, f)) as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(f.encode() + code_of(text).encode())
     return h.hexdigest()[:16]
 
 

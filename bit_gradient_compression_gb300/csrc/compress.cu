@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, LOCO_COMPRESS_STAGED_MINB(E8)) k_com
 #define LOCO_COMPRESS_ELEMS 8      // fp32 error: elements per lane (memory-bound)
 #endif
 #ifndef LOCO_COMPRESS_UNROLL_E8
-#define LOCO_COMPRESS_UNROLL_E8 1  // 8-bit error: warp tiles per iteration (64 registers: 4 CTAs per SM)
+#define LOCO_COMPRESS_UNROLL_E8 1  // 8-bit error, direct loads (LOCO_COMPRESS_STAGES_E8 = 0): warp tiles per iteration
 #endif
 #ifndef LOCO_COMPRESS_ELEMS_E8
 #define LOCO_COMPRESS_ELEMS_E8 16  // 8-bit error: elements per lane; the half-warps compute two blocks' scales at once
