@@ -119,3 +119,21 @@ def test_reference_arm_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == pytest.approx(d["value"], rel=1e-3)
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == pytest.approx(d["value"], rel=1e-3)
+
+
+def test_stored_counters_follow_kernel_code_not_comments():
+    """The stored ncu DRAM counters are keyed to each kernel's code: a comment
+    edit keeps the key, a code edit changes it, and every timed kernel has
+    its own source list."""
+    import bench
+    base = "int f(int x) {  // doubles x\n  return 2 * x; /* twice */ }\n"
+    assert bench.code_of(base) == bench.code_of("int f(int x) { // twice x\n return 2*x;   }".replace("2*x", "2 * x"))
+    assert bench.code_of(base) != bench.code_of(base.replace("2 * x", "3 * x"))
+    files = {"compress.cu": base, "decode_reduce.cu": base, "adam.cu": base, "sgd.cu": base,
+             "receiver_common.cuh": base, "device_common.cuh": base, "loco_internal.h": base}
+    h0 = bench.source_hash("adam", read=files.get)
+    h1 = bench.source_hash("adam", read=lambda f: files[f] + ("// note\n" if f == "adam.cu" else ""))
+    h2 = bench.source_hash("adam", read=lambda f: files[f] + ("int y;\n" if f == "adam.cu" else ""))
+    h3 = bench.source_hash("adam", read=lambda f: files[f] + ("int y;\n" if f == "sgd.cu" else ""))
+    assert h0 == h1 and h0 != h2 and h0 == h3
+    assert set(bench.KERNEL_SOURCES) == {"compress", "decode_reduce", "adam", "sgd"}
