@@ -586,3 +586,59 @@ def test_checkpoint_resume(L, storage):
         assert torch.equal(c, outs[k - 1][0]) and torch.equal(s, outs[k - 1][1]), k
     for a, b in zip(resumed, full):
         assert torch.equal(a, b)
+
+
+def test_concurrent_calls_on_independent_streams(L):
+    """The kernels keep no state and share no memory beyond their arguments, so
+    independent chains of calls running at the same time on four streams give
+    the bits of the same chains run one after another."""
+    n = 2 * 4096 * 8 + 123
+    chains = [dict(bits=4, block=256, W=8, e8=False, opt="adam"), dict(bits=8, block=64, W=5, e8=False, opt="sgd"),
+              dict(bits=4, block=128, W=3, e8=True, opt="adam"), dict(bits=8, block=128, W=12, e8=True, opt="sgd")]
+    hp = L.make_adam(lr=1e-3, weight_decay=0.01)
+
+    def make(i, c):
+        bits, block, W = c["bits"], c["block"], c["W"]
+        nb, cb = L.loco_num_blocks(n, block), L.loco_code_bytes(n, bits, block)
+        st = dict(cfg=L.make_config(bits=bits, block=block, beta=0.2 if c["e8"] else 0.9, reset_period=2),
+                  g=[_grad(n, torch.bfloat16, 500 + 20 * i + w) for w in range(W)],
+                  cs=[torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)],
+                  ss=[torch.empty(nb, device=DEV) for _ in range(W)], mean=torch.empty(n, device=DEV),
+                  p=wl().fill_uniform(torch.empty(n, device=DEV), 40 + i, -0.1, 0.1),
+                  m=torch.zeros(n, device=DEV), v=torch.zeros(n, device=DEV))
+        if c["e8"]:
+            st["e"] = [(torch.zeros(n, dtype=torch.int8, device=DEV), torch.zeros(nb, device=DEV)) for _ in range(W)]
+        else:
+            st["e"] = [torch.zeros(n, device=DEV) for _ in range(W)]
+        return st
+
+    def run(c, st, stream):
+        for k in (1, 2, 3):
+            for w in range(c["W"]):
+                if c["e8"]:
+                    L.loco_compress_e8(st["cfg"], st["g"][w], st["e"][w][0], st["e"][w][1], k, st["cs"][w], st["ss"][w],
+                                       stream=stream)
+                else:
+                    L.loco_compress(st["cfg"], st["g"][w], st["e"][w], k, st["cs"][w], st["ss"][w], stream=stream)
+            L.loco_decode_reduce(st["cfg"], st["cs"], st["ss"], n, st["mean"], stream=stream)
+            if c["opt"] == "adam":
+                L.loco_adam_step(st["cfg"], st["cs"], st["ss"], n, st["p"], st["m"], st["v"], hp, k, stream=stream)
+            else:
+                L.loco_sgd_step(st["cfg"], st["cs"], st["ss"], n, st["p"], 1e-2, stream=stream)
+
+    serial = [make(i, c) for i, c in enumerate(chains)]
+    for c, st in zip(chains, serial):
+        run(c, st, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    together = [make(i, c) for i, c in enumerate(chains)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in chains]
+    for c, st, s in zip(chains, together, streams):
+        with torch.cuda.stream(s):
+            run(c, st, s)
+    torch.cuda.synchronize()
+    for c, a, b in zip(chains, serial, together):
+        for key in ("mean", "p", "m", "v"):
+            assert torch.equal(a[key].view(torch.int32), b[key].view(torch.int32)), (c, key)
+        for x, y in zip(a["cs"] + a["ss"], b["cs"] + b["ss"]):
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), c
