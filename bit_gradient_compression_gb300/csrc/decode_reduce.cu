@@ -24,8 +24,8 @@ namespace loco {
 #ifndef LOCO_REDUCE_MIN_CTAS
 #define LOCO_REDUCE_MIN_CTAS 3  // CTAs per SM the stage counts are fitted for
 #endif
-#ifndef LOCO_REDUCE_CTA_MAX_W4
-#define LOCO_REDUCE_CTA_MAX_W4 0  // largest rank count whose 4-bit codes take the CTA-tile kernel
+#ifndef LOCO_REDUCE_CTA_4BIT
+#define LOCO_REDUCE_CTA_4BIT(w) 0  // rank counts whose 4-bit codes take the CTA-tile kernel (none)
 #endif
 #ifndef LOCO_REDUCE_STAGES8
 // Stages of the 8-bit kernel: two below 8 ranks; from 8 ranks one stage per
@@ -63,7 +63,7 @@ namespace loco {
 
 template <int BITS, int W>
 constexpr bool use_warp_local() {
-  return BITS == 4 && W > LOCO_REDUCE_CTA_MAX_W4;
+  return BITS == 4 && !(LOCO_REDUCE_CTA_4BIT(W));
 }
 
 // ---------------------------------------------------------------------------
