@@ -36,6 +36,20 @@ namespace loco {
 #ifndef LOCO_REDUCE_STAGES4
 #define LOCO_REDUCE_STAGES4 3
 #endif
+#ifndef LOCO_REDUCE_WL_MIN_CTAS
+// CTAs per SM the warp-local kernel is fitted for up to LOCO_REDUCE_WL_BULK_MAX_W
+// ranks: four at W = 3..6 (its registers capped at 64; 0.89-0.98 of the copy
+// rate at 2^30 elements against 0.83-0.91 with three), three at W = 7, 8 (four
+// leaves room for only two stages there: 0.82 / 0.94 against 0.91 / 0.97).
+// W = 1, 2 need fewer than 64 registers and run four either way.
+#define LOCO_REDUCE_WL_MIN_CTAS(w) ((w) >= 3 && (w) <= 6 ? 4 : LOCO_REDUCE_MIN_CTAS)
+#endif
+#ifndef LOCO_REDUCE_WL_OUT_BUFS
+// Output tiles per warp with bulk stores: two (one store in flight while the
+// next tile's means are written) measured faster at W = 2 (0.96 of the copy
+// rate against 0.94), slower at W = 1 and W = 4..8.
+#define LOCO_REDUCE_WL_OUT_BUFS(w) ((w) == 2 ? 2 : 1)
+#endif
 #ifndef LOCO_REDUCE_WL_BULK_MAX_W
 #define LOCO_REDUCE_WL_BULK_MAX_W 8  // largest rank count of the warp-local kernel with bulk output stores
 #endif
@@ -121,12 +135,14 @@ __global__ void __launch_bounds__(kThreads) k_decode_reduce(const ReduceArgs a, 
 // needs (one block per lane: E <= block) are read one tile ahead into
 // registers, or, for the rank counts LOCO_REDUCE_WL_STEPS_SMEM names, copied
 // into the stage after the codes as 8-byte pieces.  With BULK each warp writes
-// its tile's means into its own output tile in shared memory and lane 0 ships
-// it with one bulk (TMA) store; the next tile's means go there only after that
-// store has read it.
+// its tile's means into one of its own OUT_BUFS output tiles in shared memory
+// (in turn) and lane 0 ships it with one bulk (TMA) store; a tile's means go
+// into an output tile only after the store that last shipped it has read it.
 // ---------------------------------------------------------------------------
-template <int BITS, int W, int E, bool BULK, int WARPS, bool STEPS_SMEM>
+template <int BITS, int W, int E, bool BULK, int WARPS, bool STEPS_SMEM, int OUT_BUFS = 1>
 struct WarpTile {
+  static constexpr int kOutBufs = OUT_BUFS;
+  static_assert(OUT_BUFS == 1 || OUT_BUFS == 2, "one or two output tiles per warp");
   static constexpr int kWarps = WARPS;
   static constexpr bool kStepsSmem = STEPS_SMEM;
   static constexpr int WT = 32 * E;                      // elements per warp tile
@@ -136,7 +152,7 @@ struct WarpTile {
   static constexpr int kStepsMax = WT / 64;                  // steps per rank and tile, smallest block
   static constexpr size_t kStepBytes = STEPS_SMEM ? size_t(W) * kStepsMax * 4 : 0;
   static constexpr size_t kStage = size_t(W) * CB + kStepBytes;
-  static constexpr size_t kOut = BULK ? size_t(WT) * 4 : 0;  // per-warp output tile
+  static constexpr size_t kOut = BULK ? size_t(OUT_BUFS) * WT * 4 : 0;  // per-warp output tiles
   static_assert(CB % 16 == 0, "whole 16-byte pieces");
   static constexpr size_t bytes(int st) { return size_t(kWarps) * (st * kStage + kOut); }
   // Largest stage count <= want (>= 2) for which min_ctas CTAs fit on one SM.
@@ -155,8 +171,9 @@ struct WarpLocalConfig {
   static constexpr bool kLow = W <= LOCO_REDUCE_WL_BULK_MAX_W;
   static constexpr int kWarps = kLow ? 8 : LOCO_REDUCE_WL_WARPS_HI;
   static constexpr bool kBulk = kLow ? true : (LOCO_REDUCE_WL_BULK_HI != 0);
-  static constexpr int kMinCtas = kLow ? LOCO_REDUCE_MIN_CTAS : LOCO_REDUCE_WL_MIN_CTAS_HI(W);
-  using WTL = WarpTile<BITS, W, E, kBulk, kWarps, bool(LOCO_REDUCE_WL_STEPS_SMEM(W))>;
+  static constexpr int kMinCtas = kLow ? LOCO_REDUCE_WL_MIN_CTAS(W) : LOCO_REDUCE_WL_MIN_CTAS_HI(W);
+  using WTL = WarpTile<BITS, W, E, kBulk, kWarps, bool(LOCO_REDUCE_WL_STEPS_SMEM(W)),
+                      kBulk ? LOCO_REDUCE_WL_OUT_BUFS(W) : 1>;
   static constexpr int S = WTL::stages(kLow ? LOCO_REDUCE_WL_STAGES_BULK(W) : LOCO_REDUCE_WL_STAGES_HI, kMinCtas);
   static constexpr size_t kSmem = WTL::bytes(S);
   static_assert(kSmem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
@@ -173,7 +190,8 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   uint8_t* wsm = sm + size_t(warp) * S * WTL::kStage;
-  float* wout = reinterpret_cast<float*>(sm + size_t(WTL::kWarps) * S * WTL::kStage) + size_t(warp) * WTL::WT;
+  float* wout = reinterpret_cast<float*>(sm + size_t(WTL::kWarps) * S * WTL::kStage) + size_t(warp) * WTL::kOutBufs * WTL::WT;
+  [[maybe_unused]] int ob = 0;  // with two output tiles: the one the next tile's means go to
   const int64_t gw = int64_t(blockIdx.x) * WTL::kWarps + warp;
   const int64_t nw = int64_t(gridDim.x) * WTL::kWarps;
   const int64_t ntiles = a.n / WTL::WT;
@@ -239,15 +257,22 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
     float mean[E];
     mean_of_codes<BITS, W, E>(cw, sc, a.ranks.neg_zero, mean);
     if constexpr (BULK) {
-      if (lane == 0) bulk_wait_read_all();  // the previous tile's store has read the output tile
+      float* ot = wout;  // this tile's output tile
+      if constexpr (WTL::kOutBufs == 1) {
+        if (lane == 0) bulk_wait_read_all();  // the previous tile's store has read the output tile
+      } else {
+        ot = wout + ob * WTL::WT;
+        ob ^= 1;
+        if (lane == 0) bulk_wait_read<1>();  // the store before the previous one has read this output tile
+      }
       __syncwarp();
-      float4* o = reinterpret_cast<float4*>(wout + lane * E);
+      float4* o = reinterpret_cast<float4*>(ot + lane * E);
 #pragma unroll
       for (int q = 0; q < E / 4; ++q) o[q] = make_float4(mean[4 * q], mean[4 * q + 1], mean[4 * q + 2], mean[4 * q + 3]);
       fence_smem_to_async_proxy();  // this lane's means visible to the bulk copy
       __syncwarp();
       if (lane == 0) {
-        bulk_store(a.mean + tile * WTL::WT, wout, uint32_t(WTL::WT * 4));
+        bulk_store(a.mean + tile * WTL::WT, ot, uint32_t(WTL::WT * 4));
         bulk_commit();
       }
     } else {

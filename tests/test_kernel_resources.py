@@ -5,7 +5,7 @@ plus -Xptxas -v, and the assembler's per-kernel report is checked: no kernel
 spills registers or uses a stack frame, and the kernels whose measured
 occupancy depends on their register count stay within it (the int8-error
 sender and Adam within their launch bounds of 3 CTAs of 256 threads per SM,
-85 registers).
+85 registers; the warp-local 4-bit decode within its 4 or 3 CTAs per SM).
 """
 import concurrent.futures as cf
 import os
@@ -78,3 +78,10 @@ def test_register_budgets(report):
     assert len(e8) == 24 and all(r <= 85 for _, r in e8), e8
     adam = [(k, v[0]) for k, v in report.items() if "k_adam" in k]
     assert adam and all(r <= 85 for _, r in adam), [a for a in adam if a[1] > 85]
+    # the warp-local 4-bit decode k_decode_reduce_wl<4, W, 16> is fitted for four CTAs
+    # of 256 threads per SM at W = 1..6 (64 registers) and three at W = 7, 8 (85)
+    wl = {int(m.group(1)): v[0] for k, v in report.items()
+          if (m := re.search(r"k_decode_reduce_wlILi4ELi(\d+)ELi16E", k))}
+    assert sorted(wl) == list(range(1, 17)), sorted(wl)
+    assert all(wl[w] <= 64 for w in range(1, 7)), wl
+    assert all(wl[w] <= 85 for w in (7, 8)), wl

@@ -154,7 +154,7 @@ def _random_ranks(L, n, bits, block, W, seed):
 DEC_SIZES = [1, 9, 255, 1000, (1 << 16) + 3]
 
 
-@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 7, 8, 9, 13, 16])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 6, 7, 8, 9, 13, 16])
 @pytest.mark.parametrize("bits,block", [(4, 256), (4, 64), (8, 128), (8, 256)])
 def test_decode_reduce_parity(L, W, bits, block):
     cfg = L.make_config(bits=bits, block=block)
@@ -167,6 +167,24 @@ def test_decode_reduce_parity(L, W, bits, block):
         torch.cuda.synchronize()
         assert_bits_equal(mean.view().cpu().numpy(), om, f"mean n={n} W={W}")
         assert mean.intact()
+
+
+@pytest.mark.parametrize("W", range(1, 17))
+@pytest.mark.parametrize("bits,block", [(4, 256), (8, 128)])
+def test_decode_reduce_parity_several_tiles_per_warp(L, W, bits, block):
+    """2^23 + 37 elements: every warp of the persistent grid walks several
+    tiles (its pipeline stages and output tiles wrap around), then the ragged
+    tail; every rank has its own codes and steps."""
+    n = (1 << 23) + 37
+    cfg = L.make_config(bits=bits, block=block)
+    codes, scales = _random_ranks(L, n, bits, block, W, 500 + W)
+    mean = Guarded(4 * n, torch.float32)
+    L.loco_decode_reduce(cfg, codes, scales, n, mean.view())
+    om = oracle.decode_reduce([c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales], n,
+                              bits=bits, block=block, threads=8)
+    torch.cuda.synchronize()
+    assert_bits_equal(mean.view().cpu().numpy(), om, f"mean n={n} W={W}")
+    assert mean.intact()
 
 
 @pytest.mark.parametrize("W", [3, 5, 6, 7, 12, 15])
