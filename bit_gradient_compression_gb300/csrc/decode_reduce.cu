@@ -70,9 +70,10 @@ namespace loco {
 #endif
 #ifndef LOCO_REDUCE_WL_STEPS_SMEM
 // Rank counts whose tiles stage their steps with the codes (cp.async) instead
-// of reading them one tile ahead into registers: measured faster at W = 1 and
-// W > 8, slower at W = 2..8.
-#define LOCO_REDUCE_WL_STEPS_SMEM(w) ((w) == 1 || (w) > 8)
+// of reading them one tile ahead into registers: measured faster at W = 1, 3,
+// 7 and W > 8 (W = 3: 0.88 -> 0.93 of the copy rate, W = 7: 0.91 -> 0.93),
+// slower at W = 2, 4, 5, 8 (0.95 -> 0.90 at W = 2), the same at W = 6.
+#define LOCO_REDUCE_WL_STEPS_SMEM(w) ((w) == 1 || (w) == 3 || (w) == 7 || (w) > 8)
 #endif
 
 template <int BITS, int W>
