@@ -14,7 +14,11 @@ namespace loco {
 #define LOCO_ADAM_MIN_CTAS 2  // CTAs per SM the stage count is fitted for (measured best)
 #endif
 #ifndef LOCO_ADAM_STAGES
-#define LOCO_ADAM_STAGES 3
+// Stages wanted; fit_stages takes as many as fit LOCO_ADAM_MIN_CTAS CTAs per
+// SM (4 with 4-bit codes up to W = 4, 3 beyond).  Four measured faster than
+// three where they fit (4-bit, 2^30 elements: W = 1 0.93 -> 0.95 of the copy
+// rate, W = 2 0.98 -> 0.99); two were slower at every W.
+#define LOCO_ADAM_STAGES 4
 #endif
 #ifndef LOCO_ADAM_BULK
 #define LOCO_ADAM_BULK 1  // results written back into the stage and shipped by bulk (TMA) stores (0: direct stores)

@@ -13,12 +13,15 @@ namespace loco {
 #ifndef LOCO_SGD_MIN_CTAS
 // CTAs per SM the stage count is fitted for (measured best).  For 9..12 ranks
 // of 4-bit codes three CTAs would leave room for one unpipelined stage; two
-// CTAs with two stages measured faster there (W = 12: 81 % -> 88 %), but not
-// at 13..16 ranks (W = 16: 93 % with three CTAs, 87 % with two).
-#define LOCO_SGD_MIN_CTAS(bits, w) ((bits) == 4 && (w) > 8 && (w) <= 12 ? 2 : 3)
+// CTAs with two stages measured faster there (W = 12: 81 % -> 88 %), and at
+// W = 8 (three stages instead of two: 99 % -> 100 %), but not at 13..16 ranks
+// (W = 16: 93 % with three CTAs, 87 % with two) nor below 8.
+#define LOCO_SGD_MIN_CTAS(bits, w) ((bits) == 4 && (w) >= 8 && (w) <= 12 ? 2 : 3)
 #endif
 #ifndef LOCO_SGD_STAGES
-#define LOCO_SGD_STAGES 3
+// Stages wanted; fit_stages takes as many as fit (4-bit codes: 4 at W = 1).
+// Four measured faster than three where they fit (4-bit W = 1: 0.95 -> 1.00).
+#define LOCO_SGD_STAGES 4
 #endif
 #ifndef LOCO_SGD_BULK
 #define LOCO_SGD_BULK 1  // the updated param written back into the stage and shipped by a bulk (TMA) store (0: direct)

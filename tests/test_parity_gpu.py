@@ -490,6 +490,36 @@ def test_sgd_parity(L, W, bits, block, bf16_out):
                 assert pb.intact()
 
 
+@pytest.mark.parametrize("W", range(1, 17))
+@pytest.mark.parametrize("bits,block", [(4, 256), (8, 128)])
+def test_optimizer_steps_several_tiles_per_cta(L, W, bits, block):
+    """2^23 + 37 elements: every CTA of the persistent grid walks several tiles
+    (its pipeline stages wrap around, whatever stage count fits at this W),
+    then the ragged tail; one Adam(W) step and one SGD step, each rank with its
+    own codes and steps."""
+    n = (1 << 23) + 37
+    cfg = L.make_config(bits=bits, block=block)
+    codes, scales = _random_ranks(L, n, bits, block, W, 900 + W)
+    codes_h, scales_h = [c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales]
+    hpk = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, bias_correction=True,
+               eps_inside_sqrt=False)
+    p = wl().fill_uniform(torch.empty(n, device=DEV), 5, -0.05, 0.05)
+    m = wl().fill_uniform(torch.empty(n, device=DEV), 6, -1e-3, 1e-3)
+    v = wl().fill_uniform(torch.empty(n, device=DEV), 7, 0.0, 1e-6)
+    ph, mh, vh = p.cpu().numpy().copy(), m.cpu().numpy().copy(), v.cpu().numpy().copy()
+    L.loco_adam_step(cfg, codes, scales, n, p, m, v, L.make_adam(**hpk), 3)
+    oracle.adam_step(codes_h, scales_h, n, ph, mh, vh, 3, bits=bits, block=block, threads=8, **hpk)
+    torch.cuda.synchronize()
+    for got_t, want, name in ((p, ph, "param"), (m, mh, "m"), (v, vh, "v")):
+        assert_bits_equal(got_t.cpu().numpy(), want, f"adam {name} W={W}")
+    q = wl().fill_uniform(torch.empty(n, device=DEV), 8, -0.05, 0.05)
+    qh = q.cpu().numpy().copy()
+    L.loco_sgd_step(cfg, codes, scales, n, q, 3e-3)
+    oracle.sgd_step(codes_h, scales_h, n, qh, bits=bits, block=block, lr=3e-3, threads=8)
+    torch.cuda.synchronize()
+    assert_bits_equal(q.cpu().numpy(), qh, f"sgd param W={W}")
+
+
 @pytest.mark.parametrize("W", [1, 8, 13])
 @pytest.mark.parametrize("bits,block", [(4, 256), (8, 128)])
 def test_adam_bf16_parity(L, W, bits, block):
