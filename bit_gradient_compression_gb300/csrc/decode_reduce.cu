@@ -50,6 +50,28 @@ namespace loco {
 // rate against 0.94), slower at W = 1 and W = 4..8.
 #define LOCO_REDUCE_WL_OUT_BUFS(w) ((w) == 2 ? 2 : 1)
 #endif
+#ifndef LOCO_REDUCE_WL_SYNC_TILES
+#define LOCO_REDUCE_WL_SYNC_TILES(w) 0  // tiles between CTA barriers of the warp-local kernel (0: none)
+#endif
+#ifndef LOCO_REDUCE_WL_GROUP
+// Consecutive warp tiles each warp of the warp-local kernel takes in turn (1:
+// tiles gw, gw + nw, gw + 2 nw, ...; G: tiles G gw .. G gw + G-1, then the
+// group nw further on).  Over many tiles the warps drift apart, and with W > 8
+// rank streams the reads of one DRAM page then arrive from warps far apart in
+// time; a group keeps a page's reads within one warp.  W = 16: 0.85 -> 0.91 of
+// the copy rate on the 6.7G-element Llama-2-7B bucket, 0.90 -> 0.91 at 2^30.
+#define LOCO_REDUCE_WL_GROUP(w) ((w) > 8 ? 8 : 1)
+#endif
+#ifndef LOCO_REDUCE_WL_GROUP_LARGE
+// The group for buckets of at least LOCO_REDUCE_WL_GROUP_MIN_TILES warp tiles
+// per warp.  W = 8: groups of 8 gain there (0.952 -> 0.960 on the Llama-2-7B
+// bucket, 3608 tiles per warp; the same at 2^32, 2299) but lose at 2^30 (575
+// tiles per warp: 0.968 -> 0.953), so W = 8 takes them only there.
+#define LOCO_REDUCE_WL_GROUP_LARGE(w) ((w) >= 8 ? 8 : 1)
+#endif
+#ifndef LOCO_REDUCE_WL_GROUP_MIN_TILES
+#define LOCO_REDUCE_WL_GROUP_MIN_TILES 2048
+#endif
 #ifndef LOCO_REDUCE_WL_BULK_MAX_W
 #define LOCO_REDUCE_WL_BULK_MAX_W 8  // largest rank count of the warp-local kernel with bulk output stores
 #endif
@@ -180,7 +202,7 @@ struct WarpLocalConfig {
   static_assert(kSmem <= 227 * 1024, "staging area exceeds one CTA's shared memory");
 };
 
-template <int BITS, int W, int E>
+template <int BITS, int W, int E, int G>
 __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, WarpLocalConfig<BITS, W, E>::kMinCtas)
     k_decode_reduce_wl(const ReduceArgs a, int log2_block) {
   extern __shared__ __align__(16) uint8_t sm[];
@@ -234,6 +256,12 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
         if (sval[j]) cp_async8(st + sdst[j], ssrc[j] + tile * nsc);
     }
   };
+  // The tile this warp takes after `tile`.
+  constexpr int kGroup = G;
+  [[maybe_unused]] auto next_tile = [&](int64_t tile) {
+    if constexpr (kGroup == 1) return tile + nw;
+    else return (tile % kGroup != kGroup - 1) ? tile + 1 : tile + 1 + (nw - 1) * kGroup;
+  };
   // Steps of this lane's block for every rank, one tile ahead in registers.
   float sc[W];
   auto load_steps = [&](float (&s)[W], int64_t tile) {
@@ -242,15 +270,21 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
     for (int w = 0; w < W; ++w) s[w] = __ldg(a.ranks.scales[w] + blk);
   };
   if constexpr (!WTL::kStepsSmem)
-    if (gw < ntiles) load_steps(sc, gw);
-  warp_pipeline<S>(wsm, WTL::kStage, gw, nw, ntiles, issue, [&](const uint8_t* st, int64_t tile) {
+    if (gw * kGroup < ntiles) load_steps(sc, gw * kGroup);
+  // With LOCO_REDUCE_WL_SYNC_TILES = K > 0 the CTA's warps meet at a barrier
+  // after every K tiles, up to the tile count of its last warp (the fewest of
+  // any of its warps).
+  constexpr int kSync = LOCO_REDUCE_WL_SYNC_TILES(W);
+  const int64_t gw_last = int64_t(blockIdx.x) * WTL::kWarps + WTL::kWarps - 1;
+  const int64_t it_min = gw_last < ntiles ? (ntiles - gw_last + nw - 1) / nw : 0;
+  warp_pipeline<S, kSync, kGroup>(wsm, WTL::kStage, gw, nw, ntiles, issue, [&](const uint8_t* st, int64_t tile) {
     float nsc_[W];
     if constexpr (WTL::kStepsSmem) {
       const float* ss = reinterpret_cast<const float*>(st + W * WTL::CB) + ((lane * E) >> log2_block);
 #pragma unroll
       for (int w = 0; w < W; ++w) sc[w] = ss[w * WTL::kStepsMax];
     } else {
-      if (tile + nw < ntiles) load_steps(nsc_, tile + nw);
+      if (next_tile(tile) < ntiles) load_steps(nsc_, next_tile(tile));
     }
     ChunkCodes<BITS, E> cw[W];
 #pragma unroll
@@ -283,7 +317,7 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
 #pragma unroll
       for (int w = 0; w < W; ++w) sc[w] = nsc_[w];
     }
-  });
+  }, it_min);
   if constexpr (BULK)
     if (lane == 0) bulk_wait_all();
   // Elements past the last full warp tile: one warp, straight from global memory.
@@ -297,38 +331,60 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
   }
 }
 
+// Grid of the warp-local kernel with tile groups of G: resident CTAs, at most
+// one per CTA-worth of elements.
+template <int BITS, int W, int E, int G>
+cudaError_t wl_grid(const ReduceArgs& a, int* grid) {
+  using CF = WarpLocalConfig<BITS, W, E>;
+  static GridCache cache;
+  int cap = 0;
+  const cudaError_t e = grid_cap(cache, reinterpret_cast<const void*>(&k_decode_reduce_wl<BITS, W, E, G>),
+                                 CF::kWarps * 32, CF::kSmem, &cap);
+  if (e == cudaSuccess) *grid = clamp_grid(a.n, CF::kWarps * 32 * E, cap);
+  return e;
+}
+
+template <int BITS, int W, int E, int G>
+cudaError_t launch_wl(const ReduceArgs& a, int grid, cudaStream_t s) {
+  using CF = WarpLocalConfig<BITS, W, E>;
+  k_decode_reduce_wl<BITS, W, E, G><<<grid, CF::kWarps * 32, CF::kSmem, s>>>(a, ilog2_int(a.block));
+  return cudaGetLastError();
+}
+
 template <int BITS>
 struct DecodeLaunch {
   template <int W>
   struct F {
     static cudaError_t run(const ReduceArgs& a, cudaStream_t s) {
       constexpr int E = LOCO_REDUCE_ELEMS(BITS);
-      const void* fn;
-      size_t smem;
-      int threads = kThreads;
       if constexpr (use_warp_local<BITS, W>()) {
         using CF = WarpLocalConfig<BITS, W, E>;
-        fn = reinterpret_cast<const void*>(&k_decode_reduce_wl<BITS, W, E>);
-        smem = CF::kSmem;
-        threads = CF::kWarps * 32;
+        constexpr int G0 = LOCO_REDUCE_WL_GROUP(W), G1 = LOCO_REDUCE_WL_GROUP_LARGE(W);
+        int grid = 0;
+        cudaError_t e = wl_grid<BITS, W, E, G0>(a, &grid);
+        if (e != cudaSuccess) return e;
+        if constexpr (G1 != G0) {
+          // warp tiles per warp of the resident grid
+          const int64_t per_warp = (a.n / CF::WTL::WT) / (int64_t(grid) * CF::kWarps);
+          if (per_warp >= LOCO_REDUCE_WL_GROUP_MIN_TILES) {
+            e = wl_grid<BITS, W, E, G1>(a, &grid);
+            if (e != cudaSuccess) return e;
+            return launch_wl<BITS, W, E, G1>(a, grid, s);
+          }
+        }
+        return launch_wl<BITS, W, E, G0>(a, grid, s);
       } else {
         using SM = DecodeSmem<BITS, W, E>;
         static_assert(SM::kBytes <= 227 * 1024, "staging area exceeds one CTA's shared memory");
-        fn = reinterpret_cast<const void*>(&k_decode_reduce<BITS, W, E, SM::S>);
-        smem = SM::kBytes;
+        static GridCache cache;
+        int cap = 0;
+        const cudaError_t e = grid_cap(cache, reinterpret_cast<const void*>(&k_decode_reduce<BITS, W, E, SM::S>),
+                                       kThreads, SM::kBytes, &cap);
+        if (e != cudaSuccess) return e;
+        const int grid = clamp_grid(a.n, kThreads * E, cap);
+        k_decode_reduce<BITS, W, E, SM::S><<<grid, kThreads, SM::kBytes, s>>>(a, ilog2_int(a.block));
+        return cudaGetLastError();
       }
-      static GridCache cache;
-      int cap = 0;
-      const cudaError_t e = grid_cap(cache, fn, threads, smem, &cap);
-      if (e != cudaSuccess) return e;
-      const int grid = clamp_grid(a.n, threads * E, cap);
-      if constexpr (use_warp_local<BITS, W>()) {
-        k_decode_reduce_wl<BITS, W, E><<<grid, threads, smem, s>>>(a, ilog2_int(a.block));
-      } else {
-        using SM = DecodeSmem<BITS, W, E>;
-        k_decode_reduce<BITS, W, E, SM::S><<<grid, kThreads, smem, s>>>(a, ilog2_int(a.block));
-      }
-      return cudaGetLastError();
     }
   };
 };

@@ -78,10 +78,10 @@ def test_register_budgets(report):
     assert len(e8) == 24 and all(r <= 85 for _, r in e8), e8
     adam = [(k, v[0]) for k, v in report.items() if "k_adam" in k]
     assert adam and all(r <= 85 for _, r in adam), [a for a in adam if a[1] > 85]
-    # the warp-local 4-bit decode k_decode_reduce_wl<4, W, 16> is fitted for four CTAs
-    # of 256 threads per SM at W = 1..6 (64 registers) and three at W = 7, 8 (85)
-    wl = {int(m.group(1)): v[0] for k, v in report.items()
-          if (m := re.search(r"k_decode_reduce_wlILi4ELi(\d+)ELi16E", k))}
-    assert sorted(wl) == list(range(1, 17)), sorted(wl)
-    assert all(wl[w] <= 64 for w in range(1, 7)), wl
-    assert all(wl[w] <= 85 for w in (7, 8)), wl
+    # the warp-local 4-bit decode k_decode_reduce_wl<4, W, 16, group> is fitted for four
+    # CTAs of 256 threads per SM at W = 1..6 (64 registers) and three at W = 7, 8 (85)
+    wl = {(int(m.group(1)), int(m.group(2))): v[0] for k, v in report.items()
+          if (m := re.search(r"k_decode_reduce_wlILi4ELi(\d+)ELi16ELi(\d+)E", k))}
+    assert sorted({w for w, _ in wl}) == list(range(1, 17)), sorted(wl)
+    assert all(r <= 64 for (w, _), r in wl.items() if w <= 6), wl
+    assert all(r <= 85 for (w, _), r in wl.items() if w in (7, 8)), wl
