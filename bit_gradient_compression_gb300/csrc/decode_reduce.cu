@@ -54,23 +54,20 @@ namespace loco {
 #define LOCO_REDUCE_WL_SYNC_TILES(w) 0  // tiles between CTA barriers of the warp-local kernel (0: none)
 #endif
 #ifndef LOCO_REDUCE_WL_GROUP
-// Consecutive warp tiles each warp of the warp-local kernel takes in turn (1:
-// tiles gw, gw + nw, gw + 2 nw, ...; G: tiles G gw .. G gw + G-1, then the
-// group nw further on).  Over many tiles the warps drift apart, and with W > 8
-// rank streams the reads of one DRAM page then arrive from warps far apart in
-// time; a group keeps a page's reads within one warp.  W = 16: 0.85 -> 0.91 of
-// the copy rate on the 6.7G-element Llama-2-7B bucket, 0.90 -> 0.91 at 2^30.
-#define LOCO_REDUCE_WL_GROUP(w) ((w) > 8 ? 8 : 1)
-#endif
-#ifndef LOCO_REDUCE_WL_GROUP_LARGE
-// The group for buckets of at least LOCO_REDUCE_WL_GROUP_MIN_TILES warp tiles
-// per warp.  W = 8: groups of 8 gain there (0.952 -> 0.960 on the Llama-2-7B
-// bucket, 3608 tiles per warp; the same at 2^32, 2299) but lose at 2^30 (575
-// tiles per warp: 0.968 -> 0.953), so W = 8 takes them only there.
-#define LOCO_REDUCE_WL_GROUP_LARGE(w) ((w) >= 8 ? 8 : 1)
+// Consecutive warp tiles each warp of the warp-local kernel takes in turn on
+// buckets of at least LOCO_REDUCE_WL_GROUP_MIN_TILES(W) warp tiles per warp of
+// the resident grid (smaller buckets: tiles gw, gw + nw, gw + 2 nw, ...; G:
+// tiles G gw .. G gw + G-1, then the group nw further on).  Over many tiles
+// the warps drift apart, and with many rank streams the reads of one DRAM page
+// then arrive from warps far apart in time; a group keeps a page's reads within
+// one warp.  W = 16: 0.85 -> 0.91 of the copy rate on the 6.7G-element
+// Llama-2-7B bucket, 0.90 -> 0.91 at 2^30.  W = 8: 0.952 -> 0.960 on the
+// Llama-2-7B bucket (3608 tiles per warp; the same at 2^32, 2299) but 0.968 ->
+// 0.953 at 2^30 (575 tiles per warp).  Below 8 ranks: not measured faster.
+#define LOCO_REDUCE_WL_GROUP(w) ((w) >= 8 ? 8 : 1)
 #endif
 #ifndef LOCO_REDUCE_WL_GROUP_MIN_TILES
-#define LOCO_REDUCE_WL_GROUP_MIN_TILES 2048
+#define LOCO_REDUCE_WL_GROUP_MIN_TILES(w) ((w) > 8 ? 64 : 2048)
 #endif
 #ifndef LOCO_REDUCE_WL_BULK_MAX_W
 #define LOCO_REDUCE_WL_BULK_MAX_W 8  // largest rank count of the warp-local kernel with bulk output stores
@@ -359,20 +356,20 @@ struct DecodeLaunch {
       constexpr int E = LOCO_REDUCE_ELEMS(BITS);
       if constexpr (use_warp_local<BITS, W>()) {
         using CF = WarpLocalConfig<BITS, W, E>;
-        constexpr int G0 = LOCO_REDUCE_WL_GROUP(W), G1 = LOCO_REDUCE_WL_GROUP_LARGE(W);
+        constexpr int G = LOCO_REDUCE_WL_GROUP(W);
         int grid = 0;
-        cudaError_t e = wl_grid<BITS, W, E, G0>(a, &grid);
+        cudaError_t e = wl_grid<BITS, W, E, 1>(a, &grid);
         if (e != cudaSuccess) return e;
-        if constexpr (G1 != G0) {
+        if constexpr (G > 1) {
           // warp tiles per warp of the resident grid
           const int64_t per_warp = (a.n / CF::WTL::WT) / (int64_t(grid) * CF::kWarps);
-          if (per_warp >= LOCO_REDUCE_WL_GROUP_MIN_TILES) {
-            e = wl_grid<BITS, W, E, G1>(a, &grid);
+          if (per_warp >= LOCO_REDUCE_WL_GROUP_MIN_TILES(W)) {
+            e = wl_grid<BITS, W, E, G>(a, &grid);
             if (e != cudaSuccess) return e;
-            return launch_wl<BITS, W, E, G1>(a, grid, s);
+            return launch_wl<BITS, W, E, G>(a, grid, s);
           }
         }
-        return launch_wl<BITS, W, E, G0>(a, grid, s);
+        return launch_wl<BITS, W, E, 1>(a, grid, s);
       } else {
         using SM = DecodeSmem<BITS, W, E>;
         static_assert(SM::kBytes <= 227 * 1024, "staging area exceeds one CTA's shared memory");

@@ -209,8 +209,7 @@ __device__ __forceinline__ void warp_pipeline(uint8_t* wsm, size_t stage_bytes, 
       cur = (cur + 1 == S) ? 0 : cur + 1;
     }
     cp_async_wait<0>();
-    return;
-  }
+  } else {
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) {
     const int64_t tile = gw + int64_t(s) * nw;
@@ -246,6 +245,7 @@ __device__ __forceinline__ void warp_pipeline(uint8_t* wsm, size_t stage_bytes, 
     }
   }
   cp_async_wait<0>();
+  }
 }
 
 // ---------------------------------------------------------------------------
