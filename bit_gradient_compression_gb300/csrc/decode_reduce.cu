@@ -50,9 +50,6 @@ namespace loco {
 // rate against 0.94), slower at W = 1 and W = 4..8.
 #define LOCO_REDUCE_WL_OUT_BUFS(w) ((w) == 2 ? 2 : 1)
 #endif
-#ifndef LOCO_REDUCE_WL_SYNC_TILES
-#define LOCO_REDUCE_WL_SYNC_TILES(w) 0  // tiles between CTA barriers of the warp-local kernel (0: none)
-#endif
 #ifndef LOCO_REDUCE_WL_GROUP
 // Consecutive warp tiles each warp of the warp-local kernel takes in turn on
 // buckets of at least LOCO_REDUCE_WL_GROUP_MIN_TILES(W) warp tiles per warp of
@@ -268,13 +265,7 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
   };
   if constexpr (!WTL::kStepsSmem)
     if (gw * kGroup < ntiles) load_steps(sc, gw * kGroup);
-  // With LOCO_REDUCE_WL_SYNC_TILES = K > 0 the CTA's warps meet at a barrier
-  // after every K tiles, up to the tile count of its last warp (the fewest of
-  // any of its warps).
-  constexpr int kSync = LOCO_REDUCE_WL_SYNC_TILES(W);
-  const int64_t gw_last = int64_t(blockIdx.x) * WTL::kWarps + WTL::kWarps - 1;
-  const int64_t it_min = gw_last < ntiles ? (ntiles - gw_last + nw - 1) / nw : 0;
-  warp_pipeline<S, kSync, kGroup>(wsm, WTL::kStage, gw, nw, ntiles, issue, [&](const uint8_t* st, int64_t tile) {
+  warp_pipeline<S, kGroup>(wsm, WTL::kStage, gw, nw, ntiles, issue, [&](const uint8_t* st, int64_t tile) {
     float nsc_[W];
     if constexpr (WTL::kStepsSmem) {
       const float* ss = reinterpret_cast<const float*>(st + W * WTL::CB) + ((lane * E) >> log2_block);
@@ -314,7 +305,7 @@ __global__ void __launch_bounds__(WarpLocalConfig<BITS, W, E>::kWarps * 32, Warp
 #pragma unroll
       for (int w = 0; w < W; ++w) sc[w] = nsc_[w];
     }
-  }, it_min);
+  });
   if constexpr (BULK)
     if (lane == 0) bulk_wait_all();
   // Elements past the last full warp tile: one warp, straight from global memory.

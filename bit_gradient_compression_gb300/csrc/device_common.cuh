@@ -166,28 +166,25 @@ __device__ __forceinline__ void pipeline_tiles(uint8_t* sm, size_t stage_bytes, 
 
 // ---------------------------------------------------------------------------
 // Warp-local multistage pipeline.  Warp gw of nw walks its own tiles gw,
-// gw + nw, ... through S stages of its own shared memory (wsm), S-1 tiles in
-// flight while one is consumed.  The warp's lanes copy a tile together
-// (cp.async), so cp.async.wait_group (each lane's own copies landed) plus
-// __syncwarp (memory ordering among the warp's lanes) make it visible to every
-// lane; the __syncwarp also guarantees that the stage refilled next, the one
-// consumed in the previous iteration, is no longer being read.  No CTA-wide
-// barrier and no spin-wait: warps of a CTA drift freely, unless K > 0: then
-// the CTA's warps meet at a barrier after every K tiles, up to `sync_until`
-// tiles (which must not exceed the tile count of any warp of the CTA, so that
-// every warp passes the same barriers).  Every lane of the warp must run this
-// with the same arguments.
+// gw + nw, ... (or, with G > 1, groups of G consecutive tiles: G gw ..
+// G gw + G-1, then the group nw further on) through S stages of its own shared
+// memory (wsm), S-1 tiles in flight while one is consumed.  The warp's lanes
+// copy a tile together (cp.async), so cp.async.wait_group (each lane's own
+// copies landed) plus __syncwarp (memory ordering among the warp's lanes) make
+// it visible to every lane; the __syncwarp also guarantees that the stage
+// refilled next, the one consumed in the previous iteration, is no longer
+// being read.  No CTA-wide barrier and no spin-wait: warps of a CTA drift
+// freely.  Every lane of the warp must run this with the same arguments.
 //   issue(stage_base, tile): start this lane's share of the tile's copies
 //   body(stage_base, tile):  consume one staged tile
 // ---------------------------------------------------------------------------
-template <int S, int K = 0, int G = 1, typename Issue, typename Body>
+template <int S, int G = 1, typename Issue, typename Body>
 __device__ __forceinline__ void warp_pipeline(uint8_t* wsm, size_t stage_bytes, int64_t gw, int64_t nw, int64_t ntiles,
-                                              Issue issue, Body body, int64_t sync_until = 0) {
+                                              Issue issue, Body body) {
   static_assert(S >= 2, "one stage computes while the next loads");
   if constexpr (G > 1) {
-    // Tiles in groups of G consecutive ones: this warp's j-th tile is tile
-    // j % G of group gw + (j / G) * nw (next_tile gives the same order).
-    static_assert((G & (G - 1)) == 0 && K == 0, "a power-of-two group, no barriers");
+    static_assert((G & (G - 1)) == 0, "a power-of-two group");
+    // this warp's j-th tile
     auto tile_of = [&](int64_t j) { return (gw + (j / G) * nw) * G + (j % G); };
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
@@ -211,13 +208,12 @@ __device__ __forceinline__ void warp_pipeline(uint8_t* wsm, size_t stage_bytes, 
     cp_async_wait<0>();
   } else {
 #pragma unroll
-  for (int s = 0; s < S - 1; ++s) {
-    const int64_t tile = gw + int64_t(s) * nw;
-    if (tile < ntiles) issue(wsm + s * stage_bytes, tile);
-    cp_async_commit();
-  }
-  int cur = 0;
-  if constexpr (K == 0) {
+    for (int s = 0; s < S - 1; ++s) {
+      const int64_t tile = gw + int64_t(s) * nw;
+      if (tile < ntiles) issue(wsm + s * stage_bytes, tile);
+      cp_async_commit();
+    }
+    int cur = 0;
     for (int64_t tile = gw; tile < ntiles; tile += nw) {
       cp_async_wait<S - 2>();  // this lane's copies of `tile` have landed
       __syncwarp();            // ... and every other lane's; the previous stage is free
@@ -228,23 +224,7 @@ __device__ __forceinline__ void warp_pipeline(uint8_t* wsm, size_t stage_bytes, 
       body(wsm + cur * stage_bytes, tile);
       cur = (cur + 1 == S) ? 0 : cur + 1;
     }
-  } else {
-    int64_t tile = gw;
-    for (int64_t done = K; tile < ntiles; done += K) {
-      for (int k = 0; k < K && tile < ntiles; ++k, tile += nw) {
-        cp_async_wait<S - 2>();
-        __syncwarp();
-        const int prev = (cur == 0) ? S - 1 : cur - 1;
-        const int64_t ahead = tile + int64_t(S - 1) * nw;
-        if (ahead < ntiles) issue(wsm + prev * stage_bytes, ahead);
-        cp_async_commit();
-        body(wsm + cur * stage_bytes, tile);
-        cur = (cur + 1 == S) ? 0 : cur + 1;
-      }
-      if (done <= sync_until) __syncthreads();
-    }
-  }
-  cp_async_wait<0>();
+    cp_async_wait<0>();
   }
 }
 
