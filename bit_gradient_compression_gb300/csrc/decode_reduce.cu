@@ -28,10 +28,11 @@ namespace loco {
 #define LOCO_REDUCE_CTA_4BIT(w) 0  // rank counts whose 4-bit codes take the CTA-tile kernel (none)
 #endif
 #ifndef LOCO_REDUCE_STAGES8
-// Stages of the 8-bit kernel: two below 8 ranks; from 8 ranks one stage per
+// Stages of the 8-bit kernel: two below 7 ranks; from 7 ranks one stage per
 // CTA (each CTA loads, then computes, and the CTAs of an SM overlap one
-// another) measured faster (W = 12: 86 % -> 101 %; W = 2: 95 % -> 89 %).
-#define LOCO_REDUCE_STAGES8(w) ((w) >= 8 ? 1 : 2)
+// another) measured faster (W = 12: 86 % -> 101 %, W = 7: 95 % -> 99 %;
+// W = 2: 95 % -> 88 %, W = 6: 98 % -> 97 %).
+#define LOCO_REDUCE_STAGES8(w) ((w) >= 7 ? 1 : 2)
 #endif
 #ifndef LOCO_REDUCE_STAGES4
 #define LOCO_REDUCE_STAGES4 3
