@@ -188,6 +188,24 @@ def test_decode_reduce_parity_several_tiles_per_warp(L, W, bits, block):
     assert mean.intact()
 
 
+@pytest.mark.parametrize("W", range(8, 17))
+def test_decode_reduce_parity_tile_groups(L, W):
+    """2^27 + 37 elements, 4-bit codes: from W = 9 the warps of the 4-bit decode
+    take groups of 8 consecutive tiles once every warp of the resident grid has
+    at least 64 warp tiles (2^27 elements give 86-108 per warp); W = 8 keeps
+    the plain order at this size.  Every element is compared."""
+    n = (1 << 27) + 37
+    cfg = L.make_config(bits=4, block=256)
+    codes, scales = _random_ranks(L, n, 4, 256, W, 1300 + W)
+    mean = Guarded(4 * n, torch.float32)
+    L.loco_decode_reduce(cfg, codes, scales, n, mean.view())
+    om = oracle.decode_reduce([c.cpu().numpy() for c in codes], [s.cpu().numpy() for s in scales], n,
+                              bits=4, block=256, threads=8)
+    torch.cuda.synchronize()
+    assert_bits_equal(mean.view().cpu().numpy(), om, f"mean n={n} W={W}")
+    assert mean.intact()
+
+
 @pytest.mark.parametrize("W", [3, 5, 6, 7, 12, 15])
 @pytest.mark.parametrize("bits,block", [(4, 64), (8, 128)])
 def test_decode_reduce_small_steps_and_signed_zeros(L, W, bits, block):
