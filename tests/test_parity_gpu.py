@@ -173,9 +173,8 @@ def test_decode_reduce_parity(L, W, bits, block):
 @pytest.mark.parametrize("bits,block", [(4, 256), (8, 128)])
 def test_decode_reduce_parity_several_tiles_per_warp(L, W, bits, block):
     """2^25 + 37 elements: every warp of the persistent grid walks several
-    tiles, or several groups of consecutive tiles (its pipeline stages and
-    output tiles wrap around), then the ragged tail; every rank has its own
-    codes and steps."""
+    tiles (its pipeline stages and output tiles wrap around), then the ragged
+    tail; every rank has its own codes and steps."""
     n = (1 << 25) + 37
     cfg = L.make_config(bits=bits, block=block)
     codes, scales = _random_ranks(L, n, bits, block, W, 500 + W)
