@@ -54,18 +54,22 @@ namespace loco {
 #ifndef LOCO_REDUCE_WL_GROUP
 // Consecutive warp tiles each warp of the warp-local kernel takes in turn on
 // buckets of at least LOCO_REDUCE_WL_GROUP_MIN_TILES(W) warp tiles per warp of
-// the resident grid (smaller buckets: tiles gw, gw + nw, gw + 2 nw, ...; G:
-// tiles G gw .. G gw + G-1, then the group nw further on).  Over many tiles
-// the warps drift apart, and with many rank streams the reads of one DRAM page
-// then arrive from warps far apart in time; a group keeps a page's reads within
-// one warp.  W = 16: 0.85 -> 0.91 of the copy rate on the 6.7G-element
-// Llama-2-7B bucket, 0.90 -> 0.91 at 2^30.  W = 8: 0.952 -> 0.960 on the
-// Llama-2-7B bucket (3608 tiles per warp; the same at 2^32, 2299) but 0.968 ->
-// 0.953 at 2^30 (575 tiles per warp).  Below 8 ranks: not measured faster.
-#define LOCO_REDUCE_WL_GROUP(w) ((w) >= 8 ? 8 : 1)
+// the resident grid (smaller buckets, and W = 1, 2, 6: tiles gw, gw + nw,
+// gw + 2 nw, ...; G: tiles G gw .. G gw + G-1, then the group nw further on).
+// Over many tiles the warps drift apart, and the reads of one DRAM page of a
+// rank's codes then arrive from warps far apart in time; a group keeps a
+// page's reads within one warp.  Measured against the plain order (fraction of
+// the copy rate; 2^28 / 2^30 elements / the 6.7G-element Llama-2-7B bucket):
+// W = 16 0.90 -> 0.91 at 2^30, 0.85 -> 0.91 on the 7B bucket; W = 3 0.904 ->
+// 0.916 / 0.928 -> 0.937 / 0.930 -> 0.948; W = 7 0.904 -> 0.917 / 0.930 ->
+// 0.942 / 0.927 -> 0.948; W = 4, 5 the same or better.  W = 8: 0.952 -> 0.960
+// on the 7B bucket (3608 tiles per warp; the same at 2^32, 2299) but 0.968 ->
+// 0.953 at 2^30 (575), hence its higher threshold.  W = 2 (two output tiles
+// per warp) 0.967 -> 0.881 and W = 6 0.935 -> 0.920 on the 7B bucket.
+#define LOCO_REDUCE_WL_GROUP(w) ((w) == 1 || (w) == 2 || (w) == 6 ? 1 : 8)
 #endif
 #ifndef LOCO_REDUCE_WL_GROUP_MIN_TILES
-#define LOCO_REDUCE_WL_GROUP_MIN_TILES(w) ((w) > 8 ? 64 : 2048)
+#define LOCO_REDUCE_WL_GROUP_MIN_TILES(w) ((w) == 8 ? 2048 : 64)
 #endif
 #ifndef LOCO_REDUCE_WL_BULK_MAX_W
 #define LOCO_REDUCE_WL_BULK_MAX_W 8  // largest rank count of the warp-local kernel with bulk output stores

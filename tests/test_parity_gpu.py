@@ -187,13 +187,14 @@ def test_decode_reduce_parity_several_tiles_per_warp(L, W, bits, block):
     assert mean.intact()
 
 
-@pytest.mark.parametrize("W", range(8, 17))
+@pytest.mark.parametrize("W", [3, 4, 5, 7] + list(range(8, 17)))
 def test_decode_reduce_parity_tile_groups(L, W):
-    """2^27 + 37 elements, 4-bit codes: from W = 9 the warps of the 4-bit decode
-    take groups of 8 consecutive tiles once every warp of the resident grid has
-    at least 64 warp tiles (2^27 elements give 86-108 per warp); W = 8 keeps
-    the plain order at this size.  Every element is compared."""
-    n = (1 << 27) + 37
+    """2^28 + 37 elements, 4-bit codes: at W = 3, 4, 5, 7 and W > 8 the warps of
+    the 4-bit decode take groups of 8 consecutive tiles once every warp of the
+    resident grid has at least 64 warp tiles (2^28 elements give 108-216 per
+    warp); W = 8 keeps the plain order at this size.  Every element is
+    compared."""
+    n = (1 << 28) + 37
     cfg = L.make_config(bits=4, block=256)
     codes, scales = _random_ranks(L, n, 4, 256, W, 1300 + W)
     mean = Guarded(4 * n, torch.float32)
