@@ -13,7 +13,11 @@
 //    own pipeline stages (warp_pipeline) and never meets the CTA's other warps
 //    at a barrier; each warp ships its tile's means with its own bulk store.
 //    Up to 8 ranks: CTAs of 8 warps with 3 stages; beyond that the stages are
-//    larger, and CTAs of 4 warps with 2 stages keep 4-5 CTAs resident.
+//    larger, and CTAs of 4 warps with 2 stages keep 4-5 CTAs resident.  The
+//    CTAs per SM, where the steps are read, the output tiles per warp and the
+//    order in which a warp takes its tiles are fitted per W (the knobs below,
+//    each with its measurements); on large buckets a second instantiation
+//    takes the tiles in groups of consecutive ones, chosen at launch.
 #include "receiver_common.cuh"
 
 namespace loco {
